@@ -1,0 +1,255 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation, tensor
+// maps, the device status word and the kernel launches.  All validation runs
+// before any CUDA call, so a rejected call never touches the GPU.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// The library's device status word (one per device that loads the library).
+__device__ int g_status_word;
+
+// Text of the last FA_ERR_CUDA cause on this host thread.
+static thread_local char g_detail[256] = "";
+
+static int cuda_fail(const char* what, cudaError_t e) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  return FA_ERR_CUDA;
+}
+static int fail_detail(int status, const char* what) {
+  snprintf(g_detail, sizeof(g_detail), "%s", what);
+  return status;
+}
+
+Options& options() {
+  static Options o;
+  return o;
+}
+
+int* device_status_ptr() {
+  static int* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { cuda_fail("cudaGetDevice", e); return nullptr; }
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) { cuda_fail("cudaGetSymbolAddress(status word)", e); return nullptr; }
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cuda_fail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", e);
+  });
+  return fn;
+}
+
+int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_detail, sizeof(g_detail), "cuTensorMapEncodeTiled: CUresult %d", (int)r);
+    return -1;
+  }
+  return 0;
+}
+
+// sm_103 check, cached per device.
+static int check_device() {
+  static int state[64] = {};  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= 64) return fail_detail(FA_ERR_UNSUPPORTED, "device ordinal >= 64");
+  if (state[dev] == 0) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", e);
+    state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return state[dev] == 1 ? FA_OK : fail_detail(FA_ERR_UNSUPPORTED, "not an sm_103 device");
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks common to every entry point.
+static int check_shape(int B, int H, int Hkv, int N, int d) {
+  if (B < 0 || H < 1 || Hkv < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H > (1LL << 30) || N > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * ((N + 255) / 256) > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+static int check_scale(float scale) { return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG; }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_last_error_detail(void) { return g_detail; }
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_MISALIGNED: return "misaligned pointer";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_set_option(const char* key, double value) {
+  if (!key || !std::isfinite(value)) return FA_ERR_INVALID_ARG;
+  if (!std::strcmp(key, "rescale_threshold")) {
+    if (value < 0.0 || value > 64.0) return FA_ERR_INVALID_ARG;
+    options().rescale_threshold = static_cast<float>(value);
+    return FA_OK;
+  }
+  if (!std::strcmp(key, "poly_exp")) {
+    if (value != std::floor(value) || value < -1.0 || value > 32.0) return FA_ERR_INVALID_ARG;
+    options().poly_exp = static_cast<int>(value);
+    return FA_OK;
+  }
+  if (!std::strcmp(key, "bwd_2cta")) {
+    if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+    options().bwd_2cta = static_cast<int>(value);
+    return FA_OK;
+  }
+  return FA_ERR_INVALID_ARG;
+}
+
+int fa_get_option(const char* key, double* value) {
+  if (!key || !value) return FA_ERR_INVALID_ARG;
+  if (!std::strcmp(key, "rescale_threshold")) { *value = options().rescale_threshold; return FA_OK; }
+  if (!std::strcmp(key, "poly_exp")) { *value = options().poly_exp; return FA_OK; }
+  if (!std::strcmp(key, "bwd_2cta")) { *value = options().bwd_2cta; return FA_OK; }
+  return FA_ERR_INVALID_ARG;
+}
+
+int fa_last_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  int* p = device_status_ptr();
+  if (!p) return FA_ERR_CUDA;
+  int v = 0;
+  if ((e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail("cudaMemcpy", e);
+  const int zero = 0;
+  if (v != 0 && (e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail("cudaMemcpy", e);
+  return v;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+           int causal, float scale, void* stream) {
+  int st = check_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (B == 0 || N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+
+  CUtensorMap tq, tk, tv;
+  if (make_tmap_bf16_rows(&tq, q, d, N, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, N, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tv, v, d, N, (long long)B * Hkv))
+    return FA_ERR_CUDA;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.tau = options().rescale_threshold;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic) {
+  if (check_shape(B, H, Hkv, N, d)) return 0;
+  const size_t rows = (size_t)B * H * N;
+  size_t bytes = rows * d * 4 + rows * 4;  // dQ accumulator + D
+  bytes = (bytes + 255) & ~size_t(255);
+  if (deterministic) bytes += ((size_t)B * H * ((N + 127) / 128) * 4 + 255) & ~size_t(255);
+  return bytes;
+}
+
+int fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int Hkv, int N, int d, int deterministic,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  (void)o; (void)dout; (void)B; (void)H; (void)Hkv; (void)N; (void)d; (void)deterministic;
+  (void)workspace; (void)workspace_bytes; (void)stream;
+  return FA_ERR_UNSUPPORTED;
+}
+
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse, void* dk, void* dv,
+                int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  (void)q; (void)k; (void)v; (void)dout; (void)lse; (void)dk; (void)dv; (void)B; (void)H; (void)Hkv; (void)N;
+  (void)d; (void)causal; (void)scale; (void)deterministic; (void)workspace; (void)workspace_bytes; (void)stream;
+  return FA_ERR_UNSUPPORTED;
+}
+
+int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, float scale, int deterministic,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  (void)dq; (void)B; (void)H; (void)Hkv; (void)N; (void)d; (void)scale; (void)deterministic; (void)workspace;
+  (void)workspace_bytes; (void)stream;
+  return FA_ERR_UNSUPPORTED;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
+           void* workspace, size_t workspace_bytes, void* stream) {
+  int st = fa_bwd_preprocess(o, dout, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
+  if (st) return st;
+  st = fa_bwd_main(q, k, v, dout, lse, dk, dv, B, H, Hkv, N, d, causal, scale, deterministic, workspace,
+                   workspace_bytes, stream);
+  if (st) return st;
+  return fa_bwd_postprocess(dq, B, H, Hkv, N, d, scale, deterministic, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

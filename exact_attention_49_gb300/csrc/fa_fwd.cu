@@ -1,0 +1,341 @@
+// fa_fwd.cu -- exact attention forward for sm_103a.
+//
+// One CTA owns two query tiles of 128 rows (256 consecutive rows of one head)
+// and walks the key/value tiles of 128 rows of that head:
+//
+//   tiling      -- "FlashAttention" wiki note, 定義 item (1); the explainer's
+//                  tiling paragraph (blocks loaded from HBM into on-chip memory,
+//                  local scores computed there, no N x N matrix in HBM);
+//   online softmax with rescale when the running max grows -- the explainer's
+//                  online-softmax paragraph;
+//   asynchronous MMA, warp specialisation, TMA -- wiki sections FA3 (1), FA4 (1);
+//   conditional rescale -- FA4 summary (ai-papers.net), 提案手法 item 2, and the
+//                  wiki's FA4 (2): the O/l correction is skipped unless the row
+//                  max has grown by more than tau (log2 units) since the value
+//                  the exponentials are taken against; the result is exact
+//                  because O and l always share that reference max.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp 8     MMA issuer (one thread) and TMEM allocator
+//   warp 9     TMA producer (one thread)
+// Tensor memory (512 columns): S0 | S1 | O0 | O1; P (bf16) overwrites the first
+// half of its S block and feeds the PV MMA straight from TMEM.
+// Shared memory: Q0, Q1 and a ring of K/V tiles (K_j and V_j take turns).
+#include "fa_internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                    // rows per query tile
+  static constexpr int BN = 128;                    // keys per K/V tile
+  static constexpr int TILE = 128 * D * 2;          // bytes of one 128 x D bf16 tile
+  static constexpr int CHUNKS = D / 64;             // 128-byte swizzle atoms across D
+  static constexpr int STAGES = (D == 128) ? 4 : 8; // K/V ring slots
+  static constexpr int SMEM_Q = 2 * TILE;
+  static constexpr int SMEM_RING = STAGES * TILE;
+  static constexpr int NBAR = 2 * STAGES + 8;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::SMEM_Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + C::SMEM_RING);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  const uint32_t q_full = bar0 + 8u * (2 * C::STAGES);
+  auto s_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 1 + w); };
+  auto p_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 3 + w); };
+  auto o_bar = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 5 + w); };
+  const uint32_t mma_done = bar0 + 8u * (2 * C::STAGES + 7);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // ---- work unit: (b, h, block of 256 query rows); causal: heaviest blocks first
+  const int N = p.N;
+  const int ncb = (N + 255) / 256;
+  const int BH = p.B * p.H;
+  const int t = blockIdx.x;
+  const int cb = p.causal ? (ncb - 1 - t / BH) : (t / BH);
+  const int bh = t % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  const int g = h / (p.H / p.Hkv);
+  const int q0 = cb * 256;
+  const int n_kv_all = (N + 127) / 128;
+  const int n_kv = p.causal ? min(n_kv_all, (q0 + 256) / 128) : n_kv_all;
+  const int kv_z = b * p.Hkv + g;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(q_full, 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(s_full(w), 1);
+      mbar_init(p_full(w), 128);
+      mbar_init(o_bar(w), 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 9 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      for (int qt = 0; qt < 2; ++qt)
+        for (int ch = 0; ch < C::CHUNKS; ++ch)
+          tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, q0 + qt * 128, bh);
+      int issued = 0;
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int slot = it % C::STAGES;
+        if (!mbar_wait(empty_bar(slot), ((it / C::STAGES) & 1) ^ 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(full_bar(slot), C::TILE);
+        for (int ch = 0; ch < C::CHUNKS; ++ch)
+          tma_load_3d(smem_u32(sRing + slot * C::TILE + ch * 16384), (it & 1) ? &tm_v : &tm_k, full_bar(slot),
+                      ch * 64, (it >> 1) * 128, kv_z);
+        issued = it + 1;
+      }
+      if (*abort) {
+        // The CTA gave up: let the copies still in flight land before the CTA
+        // exits (each completes its slot's phase), bounded at 1 ms per copy.
+        for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(full_bar(it % C::STAGES), (it / C::STAGES) & 1) && globaltimer() - t0 < 1000000ull) {
+          }
+        }
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(q_full, 0) && globaltimer() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t ring = smem_u32(sRing);
+      auto issue_s = [&](int w, int slot) {
+        const uint32_t a0 = q_addr + w * C::TILE, b0 = ring + slot * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + (w ? C::COL_S1 : C::COL_S0), sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                 idS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int w, int slot, bool acc) {
+        const uint32_t v0 = ring + slot * C::TILE;
+        const uint32_t sc = w ? C::COL_S1 : C::COL_S0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + (w ? C::COL_O1 : C::COL_O0), tmem + sc + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
+                 idO, (acc || kk > 0) ? 1u : 0u);
+      };
+      auto slot_of = [&](int it) { return it % C::STAGES; };
+      auto par_of = [&](int it) { return (uint32_t)((it / C::STAGES) & 1); };
+      bool ok = mbar_wait(q_full, 0, abort, p.status);
+      if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), abort, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, slot_of(0));
+        mma_commit(s_full(0));
+        issue_s(1, slot_of(0));
+        mma_commit(s_full(1));
+        mma_commit(empty_bar(slot_of(0)));
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int itv = 2 * j + 1, itk = 2 * j + 2;
+        if (!(ok = mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status))) break;
+        if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
+        tc_fence_after();
+        issue_pv(0, slot_of(itv), j > 0);
+        mma_commit(o_bar(0));
+        const bool more = j + 1 < n_kv;
+        if (more) {
+          if (!(ok = mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status))) break;
+          tc_fence_after();
+          issue_s(0, slot_of(itk));
+          mma_commit(s_full(0));
+        }
+        if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+        tc_fence_after();
+        issue_pv(1, slot_of(itv), j > 0);
+        mma_commit(o_bar(1));
+        mma_commit(empty_bar(slot_of(itv)));
+        if (more) {
+          issue_s(1, slot_of(itk));
+          mma_commit(s_full(1));
+          mma_commit(empty_bar(slot_of(itk)));
+        }
+      }
+      // drain: every MMA issued above has finished before TMEM is released
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int w = warp >> 2;            // query tile
+    const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
+    const int row = q0 + w * 128 + r;   // absolute query position
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (w ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = tmem + lane_off + (w ? C::COL_O1 : C::COL_O0);
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;  // reference max (log2 units) of O and l
+    float l = 0.f;
+    bool ok = true;
+    const int tile_row0 = q0 + w * 128;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tS + 32 * c, rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
+      }
+      const int col0 = j * 128;
+      if ((p.causal && col0 + 127 > tile_row0) || col0 + 128 > N) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int col = col0 + c;
+          if ((p.causal && col > row) || col >= N) s[c] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * sl2;
+      const bool need = m_tile > m_used + p.tau;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? m_tile : m_used;
+        const float alpha = need ? ex2_mufu(m_used - m_new) : 1.f;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds sum_{j'<j} P V against m_used; it must be complete before rescaling
+          ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (j - 1) & 1, abort, p.status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t rr[16];
+            tmem_ld16(tO + 16 * c, rr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st16(tO + 16 * c, rr);
+          }
+          tmem_st_wait();
+        }
+        l *= alpha;
+        m_used = m_new;
+      }
+      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_mufu(fmaf(s[32 * c + 2 * i], sl2, neg_m));
+          const float p1 = ex2_mufu(fmaf(s[32 * c + 2 * i + 1], sl2, neg_m));
+          l += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full(w));
+    }
+    // ---- epilogue: O / l -> bf16, LSE = ln 2 * (m_used + log2 l)
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (n_kv - 1) & 1, abort, p.status));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * N + row) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tO + 32 * c, rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+        if (row < N) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            orow[c * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (row < N) p.lse[(size_t)bh * N + row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const long long blocks = (long long)((p.N + 255) / 256) * p.B * p.H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  fwd_kernel<D><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, stream);
+  return launch_fwd_d<128>(tq, tk, tv, p, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,40 @@
+// fa_internal.h -- host-side declarations shared by the C-ABI file and the
+// kernel files (launchers and parameter blocks).  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+// Runtime-tunable switches (set through fa_set_option).
+struct Options {
+  float rescale_threshold = 8.0f;  // tau, log2 units: skip the O/l rescale unless the row max grows by more
+  int poly_exp = -1;               // exp2 split: -1 = default, else columns of every 32 on the FMA polynomial
+  int bwd_2cta = 1;                // reserved switch for the paired-CTA backward
+};
+Options& options();
+
+struct FwdParams {
+  void* o;           // bf16 [B,H,N,d]
+  float* lse;        // fp32 [B,H,N], natural log
+  int B, H, Hkv, N;
+  int causal;
+  float scale_log2;  // softmax scale * log2(e)
+  float tau;         // rescale threshold, log2 units
+  int* status;       // device status word
+};
+
+// Launch the forward kernel for head dim d (64 or 128).  Returns a cudaError_t.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream);
+
+// Build a 3-D bf16 tensor map over a contiguous [outer][rows][d] array with a
+// box of 64 x 128 x 1 elements and 128-byte swizzle.  Returns 0 on success.
+int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer);
+
+// Device address of the library's status word on the current device (nullptr on error).
+int* device_status_ptr();
+
+}  // namespace fa

@@ -1,0 +1,133 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) IO-aware exact attention library.
+ *
+ * What it computes.  Exact scaled-dot-product attention, not an approximation
+ * ("FlashAttention" wiki note, notes.yuuk.io, section 定義): for every batch b,
+ * query head h and query row i, with K/V head g = h / (H / Hkv),
+ *
+ *     S_ij  = scale * <q_i, k_j>,  S_ij = -inf for j > i when causal
+ *     P_ij  = exp(S_ij - LSE_i),   LSE_i = log sum_j exp(S_ij)
+ *     O_i   = sum_j P_ij v_j
+ *
+ * The forward never stores the N x N matrix S or P in device memory: it tiles
+ * Q/K/V through on-chip memory with an online softmax (section 定義 item (1);
+ * the tiling and online-softmax paragraphs of the singularity-lens.com
+ * explainer).  The backward recomputes P from the saved LSE on chip (定義
+ * item (2); the explainer's recomputation paragraph) and returns the gradients
+ * of L = sum(O * dO):
+ *
+ *     dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P * (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q   (dK, dV summed over the query
+ *     heads that share a K/V head).
+ *
+ * Layouts (row-major, contiguous, no padding):
+ *     q, o, dout, dq   bf16  [B][H][N][d]
+ *     k, v, dk, dv     bf16  [B][Hkv][N][d]
+ *     lse              fp32  [B][H][N], natural logarithm
+ * Causal masking is top-left aligned (query i sees keys 0..i).
+ *
+ * Ownership.  The caller allocates every buffer on the current CUDA device,
+ * including the backward workspace (size from fa_bwd_workspace_bytes).  The
+ * library allocates no device memory and keeps no pointer after a call.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Calls enqueue work and return; they do not synchronise.
+ *
+ * Errors.  Every argument is validated before anything is launched, so a call
+ * that returns FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED or
+ * FA_ERR_WORKSPACE has not touched the GPU.  FA_ERR_CUDA reports a launch or
+ * driver error (cudaGetLastError is left as CUDA set it).  A device-side wait
+ * that gives up (bounded at about 2 s) records FA_ERR_DEVICE_TIMEOUT in a
+ * device status word, read and cleared by fa_last_device_status.
+ *
+ * Supported: d in {64, 128}; H % Hkv == 0; 16-byte aligned bf16 pointers,
+ * 4-byte aligned lse; N >= 0, any N for the forward, N % 128 == 0 for the
+ * backward; scale finite and > 0; an sm_103 device.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,     /* null pointer, bad size, H % Hkv != 0, bad scale */
+  FA_ERR_UNSUPPORTED = -2,     /* d not in {64,128}, N not supported, not an sm_103 device */
+  FA_ERR_MISALIGNED = -3,      /* a pointer is not aligned as required */
+  FA_ERR_WORKSPACE = -4,       /* workspace missing or smaller than fa_bwd_workspace_bytes */
+  FA_ERR_CUDA = -5,            /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait gave up */
+} fa_status;
+
+/* Forward: o = softmax(scale * q k^T [causal mask]) v, lse = row logsumexp.
+ * Inputs q [B,H,N,d], k/v [B,Hkv,N,d] bf16; outputs o bf16 [B,H,N,d] and
+ * lse fp32 [B,H,N].  One kernel launch on `stream`. */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
+ * [B,H,N,d], the fp32 row terms D [B,H,N], and (deterministic mode) one
+ * int32 ordering counter per (b, h, 128-row query block).  0 on bad sizes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic);
+
+/* Backward: dq, dk, dv (bf16) from q, k, v, o, dout (bf16) and lse (fp32, as
+ * written by fa_fwd).  deterministic = 1 makes the dQ accumulation order fixed
+ * so repeated calls give bit-identical results (FA4's deterministic backward
+ * mode, named in the wiki's 未解決の問い section).  Runs fa_bwd_preprocess,
+ * fa_bwd_main and fa_bwd_postprocess on `stream`. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv,
+           int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three stages of fa_bwd, exposed so that callers (and the benchmark) can
+ * time or schedule them separately.  Same arguments and checks as fa_bwd.
+ *   preprocess : D_i = sum_c dO_ic O_ic (fp32), zero the dQ accumulator and counters
+ *   main       : recompute P from LSE tile by tile; dK, dV written; dQ accumulated
+ *   postprocess: dQ = scale * accumulator, rounded to bf16 */
+int fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int Hkv, int N, int d,
+                      int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, float scale,
+                       int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Ablation switches (process-wide; take effect on the next call):
+ *   "rescale_threshold"  tau >= 0 in log2 units (default 8): the running-max
+ *                        correction of O and l is skipped unless the row max
+ *                        grew by more than tau (FA4 conditional rescaling,
+ *                        ai-papers.net summary, 提案手法 item 2).  0 rescales
+ *                        whenever the max grows.
+ *   "poly_exp"           exp2 split between the MUFU unit and an FMA-pipe
+ *                        polynomial (wiki FA4 (2)): number of columns out of
+ *                        every 32 computed by the polynomial, 0..32; -1 = default.
+ * Returns FA_OK or FA_ERR_INVALID_ARG (unknown key or value out of range). */
+int fa_set_option(const char* key, double value);
+int fa_get_option(const char* key, double* value);
+
+/* Static description of a status code; never NULL. */
+const char* fa_status_string(int status);
+
+/* Synchronise `stream`, then return and clear the device status word:
+ * FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the
+ * last call, or FA_ERR_CUDA if the synchronisation itself failed. */
+int fa_last_device_status(void* stream);
+
+/* Text describing the cause of the last FA_ERR_CUDA / FA_ERR_UNSUPPORTED
+ * returned on the calling host thread (the failing call and CUDA's error
+ * string); "" if none.  Owned by the library, valid until the next call. */
+const char* fa_last_error_detail(void);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,97 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function that include/fa.h declares, and rejects bad arguments with the
+documented status code before touching any GPU (these calls run on machines
+with no GPU at all)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_attention_49_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_set_option",
+                     "fa_status_string", "fa_last_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    from exact_attention_49_gb300 import binding as fa
+    assert fa.fa_version() >= 100
+    for code in range(-6, 1):
+        assert fa.status_string(code) not in ("", "unknown status")
+    assert fa.status_string(42) == "unknown status"
+
+
+def test_options_roundtrip(L):
+    from exact_attention_49_gb300 import binding as fa
+    old = fa.fa_get_option("rescale_threshold")
+    assert fa.fa_set_option("rescale_threshold", 0.0) == fa.FA_OK
+    assert fa.fa_get_option("rescale_threshold") == 0.0
+    assert fa.fa_set_option("rescale_threshold", old) == fa.FA_OK
+    assert fa.fa_set_option("rescale_threshold", -1.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("poly_exp", 33) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("poly_exp", 2.5) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("no_such_option", 1.0) == fa.FA_ERR_INVALID_ARG
+
+
+P = ctypes.c_void_p
+GOOD = P(1 << 20)          # never dereferenced: every case below fails validation first
+BAD = P((1 << 20) + 8)     # 8-byte aligned only
+
+
+def fwd(L, q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, B=1, H=2, Hkv=1, N=128, d=64, causal=0, scale=0.125):
+    return L.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, None)
+
+
+def test_fwd_validation(L):
+    from exact_attention_49_gb300 import binding as fa
+    assert fwd(L, q=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, lse=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, H=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(L, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(L, q=BAD) == fa.FA_ERR_MISALIGNED
+    assert fwd(L, o=BAD) == fa.FA_ERR_MISALIGNED
+    assert fwd(L, lse=P((1 << 20) + 2)) == fa.FA_ERR_MISALIGNED
+    assert fwd(L, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, B=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, N=-5) == fa.FA_ERR_INVALID_ARG
+    # empty problems are valid and launch nothing, even with NULL pointers
+    assert fwd(L, N=0, q=None, k=None, v=None, o=None, lse=None) == fa.FA_OK
+    assert fwd(L, B=0, q=None, k=None, v=None, o=None, lse=None) == fa.FA_OK
+
+
+def test_workspace_size(L):
+    from exact_attention_49_gb300 import binding as fa
+    B, H, N, d = 2, 4, 256, 64
+    ws = fa.fa_bwd_workspace_bytes(B, H, 2, N, d, 0)
+    assert ws >= B * H * N * d * 4 + B * H * N * 4
+    assert fa.fa_bwd_workspace_bytes(B, H, 2, N, d, 1) > ws
+    assert fa.fa_bwd_workspace_bytes(B, 3, 2, N, d, 0) == 0
+    assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 96, 0) == 0

@@ -1,0 +1,133 @@
+"""GPU parity of fa_fwd against the fp64 CPU oracle on the same seeded bf16 inputs.
+
+Small cases are checked element by element on every row; the full-size
+workloads (B4 H16 N8192 d128 causal, its Q,K x4 variant, the GQA B2 Hq32 Hkv8
+N16384 workload and the long-context sweep) run on the GPU at full size, in
+the launch configuration the benchmark times, and are checked on sampled heads
+(every row) or, for the sweep, on sampled rows of every head (rows of the
+forward are independent, so the sample is exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_49_gb300 import binding as fa
+from exact_attention_49_gb300.inputs import WORKLOADS, long_context, make_inputs
+from oracle import reference as ref
+from parity import LSE_TOL, O_TOL, max_abs, o_error, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_attention_49_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+
+
+def run_fwd(q, k, v, causal, scale):
+    o, lse = fa.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    return o, lse
+
+
+def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0):
+    q, k, v, _ = make_inputs(B, H, Hkv, N, d, seed, qk_mult)
+    scale = d ** -0.5
+    o, lse = run_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = ref.attn_fwd(to64(q), to64(k), to64(v), causal, scale)
+    eo, el = o_error(to64(o), o_ref), max_abs(to64(lse), lse_ref)
+    assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
+    return eo, el
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [128, 256, 384, 1024])
+def test_fwd_small(N, causal, d):
+    check_full(1, 2, 2, N, d, causal, seed=100 + N + d)
+
+
+def test_fwd_c1():
+    w = WORKLOADS["C1"]
+    check_full(w.B, w.H, w.Hkv, w.N, w.d, w.causal, w.seed)
+
+
+def test_fwd_c2():
+    w = WORKLOADS["C2"]
+    check_full(w.B, w.H, w.Hkv, w.N, w.d, w.causal, w.seed)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_gqa_small(causal, d):
+    check_full(2, 8, 2, 512, d, causal, seed=7)
+
+
+@pytest.mark.parametrize("N", [1, 17, 127, 129, 200, 255, 257, 333, 700])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_ragged(N, causal):
+    for d in (64, 128):
+        check_full(1, 3, 1, N, d, causal, seed=N)
+
+
+def test_fwd_empty():
+    z = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    assert fa.fa_fwd(z, z, z, z, z, 1, 2, 2, 0, 64, 1, 0.125) == fa.FA_OK
+    assert fa.fa_fwd(z, z, z, z, z, 0, 2, 2, 128, 64, 1, 0.125) == fa.FA_OK
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0])
+def test_fwd_rescale_threshold(tau):
+    old = fa.fa_get_option("rescale_threshold")
+    try:
+        assert fa.fa_set_option("rescale_threshold", tau) == fa.FA_OK
+        check_full(1, 4, 4, 2048, 128, True, seed=11, qk_mult=4.0)
+        check_full(1, 4, 4, 1024, 64, False, seed=12, qk_mult=4.0)
+    finally:
+        fa.fa_set_option("rescale_threshold", old)
+
+
+def _heads_sample(B, H, seed, n=4):
+    rng = np.random.default_rng(seed)
+    pick = {(0, 0), (B - 1, H - 1)}
+    while len(pick) < min(n, B * H):
+        pick.add((int(rng.integers(B)), int(rng.integers(H))))
+    return sorted(pick)
+
+
+def check_big_heads(w):
+    q, k, v, _ = make_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.seed, w.qk_mult)
+    o, lse = run_fwd(q, k, v, w.causal, w.scale)
+    grp = w.H // w.Hkv
+    for b, h in _heads_sample(w.B, w.H, w.seed):
+        g = h // grp
+        o_ref, lse_ref = ref.attn_fwd(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, g:g + 1]),
+                                      to64(v[b:b + 1, g:g + 1]), w.causal, w.scale)
+        eo = o_error(to64(o[b:b + 1, h:h + 1]), o_ref)
+        el = max_abs(to64(lse[b:b + 1, h:h + 1]), lse_ref)
+        assert eo <= O_TOL and el <= LSE_TOL, ((b, h), eo, el)
+
+
+@pytest.mark.parametrize("name", ["C3", "C3b", "C4"])
+def test_fwd_full_size_sampled_heads(name):
+    check_big_heads(WORKLOADS[name])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 8192, 16384, 32768, 65536])
+def test_fwd_long_context_sampled_rows(N, d):
+    w = long_context(N, d)
+    q, k, v, _ = make_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.seed)
+    o, lse = run_fwd(q, k, v, True, w.scale)
+    rng = np.random.default_rng(N + d)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(N - 128, N), rng.integers(0, N, 256)]))
+    heads = [0, 5, 10, 15]
+    qs = q[:, heads][:, :, rows]
+    o_ref, lse_ref = ref.attn_fwd(to64(qs), to64(k[:, heads]), to64(v[:, heads]), True, w.scale, qpos=rows)
+    eo = o_error(to64(o[:, heads][:, :, rows]), o_ref)
+    el = max_abs(to64(lse[:, heads][:, :, rows]), lse_ref)
+    assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
