@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path (forward + backward) on GB300.
+
+One step = fa_fwd + fa_bwd (preprocess, main, postprocess) over the causal
+B=4, H=16, N=8192, d=128 bf16 workload (the configuration the throughput
+target is quoted on), inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x the
+forward.  Multi-GPU: one process per GPU (torchrun), each runs an independent
+replica of the workload (the method has no exchange step); value = all
+replicas' FLOPs / the slowest rank's time.
+
+The reference arm (--impl reference) is the fp64 CPU oracle on the host cores,
+timed on a bounded sample (whole heads) of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+NOMINAL_PEAK_TFLOPS = 2250.0
+
+
+def flops_fwd(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "fwd": ["exact_attention_49_gb300/csrc/fa_fwd.cu", "exact_attention_49_gb300/csrc/sm103.cuh"],
+    "bwd_main": ["exact_attention_49_gb300/csrc/fa_bwd.cu", "exact_attention_49_gb300/csrc/sm103.cuh"],
+}
+
+
+def dram_traffic(kernel):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("bytes_per_launch_full_workload")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(w, q, k, v, do, budget_s=12.0, max_heads=8):
+    """Time the fp64 oracle (fwd + bwd) on whole heads of the workload, one K/V
+    group at a time, until about budget_s seconds of CPU work; returns
+    (TFLOP/s, seconds, heads, threads)."""
+    from oracle import reference as ref
+    grp = w.H // w.Hkv
+    f_head = flops_fwd(1, 1, w.N, w.d, w.causal) * 3.5
+    t0 = time.perf_counter()
+    heads = 0
+    g = 0
+    while heads < max_heads:
+        b, kv = divmod(g, w.Hkv)
+        if b >= w.B:
+            break
+        hs = slice(kv * grp, (kv + 1) * grp)
+        q64 = q[b:b + 1, hs].double().numpy()
+        k64 = k[b:b + 1, kv:kv + 1].double().numpy()
+        v64 = v[b:b + 1, kv:kv + 1].double().numpy()
+        do64 = do[b:b + 1, hs].double().numpy()
+        ref.attn_fwd(q64, k64, v64, w.causal, w.scale)
+        ref.attn_bwd(q64, k64, v64, do64, w.causal, w.scale)
+        heads += grp
+        g += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return f_head * heads / dt / 1e12, dt, heads, ref.num_threads()
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import torch
+    from exact_attention_49_gb300.inputs import workload_inputs
+    from oracle import reference as ref
+    q, k, v, do = workload_inputs(w)
+    grp = w.H // w.Hkv
+    f_step = flops_fwd(1, grp, w.N, w.d, w.causal) * 3.5
+    q64 = q[0:1, 0:grp].double().numpy()
+    k64 = k[0:1, 0:1].double().numpy()
+    v64 = v[0:1, 0:1].double().numpy()
+    do64 = do[0:1, 0:grp].double().numpy()
+
+    def step():
+        ref.attn_fwd(q64, k64, v64, w.causal, w.scale)
+        ref.attn_bwd(q64, k64, v64, do64, w.causal, w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    val = f_step * args.steps / dt / 1e12
+    sample = ("one K/V group (%d query head%s) of the workload, forward + backward, per step"
+              % (grp, "" if grp == 1 else "s"))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": ref.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name + ", forward + backward", "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
+            "d": w.d, "causal": w.causal, "softmax_scale": "1/sqrt(d)", "seed": w.seed,
+            "inputs": "Q,K,V,dO i.i.d. N(0,1) rounded to bf16",
+            "l2": "inputs larger than L2: each of Q,K,V,O,dO,dQ,dK,dV is %d MiB (L2 is 129 MB)"
+                  % (w.B * w.H * w.N * w.d * 2 >> 20),
+            "parallelism": "replicas"}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_49_gb300 import binding as fa
+    from exact_attention_49_gb300.inputs import workload_inputs
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fa.lib()
+    dev = torch.device("cuda", local)
+    q_h, k_h, v_h, do_h = workload_inputs(w)
+    B, H, Hkv, N, d, causal, scale = w.B, w.H, w.Hkv, w.N, w.d, int(w.causal), w.scale
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    det = int(args.deterministic)
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, det)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def check(name, st):
+        if st != fa.FA_OK:
+            raise fa.FAError(name, st)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        check("fa_fwd", fa.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream))
+        if e is not None:
+            e[1].record(stream)
+        check("fa_bwd_preprocess", fa.fa_bwd_preprocess(o, do, lse, B, H, Hkv, N, d, det, wsp, ws_bytes, stream))
+        if e is not None:
+            e[2].record(stream)
+        check("fa_bwd_main", fa.fa_bwd_main(q, k, v, do, lse, dk, dv, B, H, Hkv, N, d, causal, scale, det, wsp,
+                                            ws_bytes, stream))
+        if e is not None:
+            e[3].record(stream)
+        check("fa_bwd_postprocess", fa.fa_bwd_postprocess(dq, B, H, Hkv, N, d, det, wsp, ws_bytes, stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise fa.FAError("device status after warm-up", st)
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+    clocks = clk.summary()
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise fa.FAError("device status after the timed steps", st)
+    total_ms = start.elapsed_time(stop)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    main_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    f_fwd = flops_fwd(B, H, N, d, w.causal)
+    f_bwd = 2.5 * f_fwd
+    value = (f_fwd + f_bwd) * ws * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hdo = (x.pin_memory() for x in (q_h, k_h, v_h, do_h))
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q_h, q_h, k_h, v_h))
+    hlse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = (f_fwd + f_bwd) * ws * e2e_steps / (float(e2e_ms.item()) * 1e-3) / 1e12
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    timed_s = total_ms * 1e-3
+    peak_key = "bf16_tflops_sustained" if timed_s > 1.0 else "bf16_tflops"
+    peak = float(peaks[peak_key])
+    dominant = "bwd_main" if main_ms >= fwd_ms else "fwd"
+    dom_ms = main_ms if dominant == "bwd_main" else fwd_ms
+    dom_flops = f_bwd if dominant == "bwd_main" else f_fwd
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": dram_traffic(dominant),
+                "peak_source": "%s %s (%s)" % (peak_src, peak_key, "MEASURED_PEAKS.json" if peak_src == "measured"
+                                               else "profiling recipe fallback")}
+
+    # ---- CPU baseline: the oracle on this host's cores, bounded sample
+    cpu_val, cpu_s, cpu_heads, cores = cpu_oracle_sample(w, q_h, k_h, v_h, do_h, budget_s=args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+        "pct_of_peak": {"measured_bf16": value / ws / peak, "nominal_2250": value / ws / NOMINAL_PEAK_TFLOPS},
+        "fwd": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                "frac_of_nominal_2250": f_fwd / (fwd_ms * 1e-3) / 1e12 / NOMINAL_PEAK_TFLOPS},
+        "bwd": {"ms": ms_step - fwd_ms, "tflops": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12,
+                "main_ms": main_ms,
+                "frac_of_nominal_2250": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12 / NOMINAL_PEAK_TFLOPS},
+        "deterministic": bool(det),
+        "roofline": roofline,
+        "cpu_baseline": {"value": cpu_val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d whole heads (forward + backward, fp64) of the workload, %.1f s"
+                                   % (cpu_heads, cpu_s)},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="C3")
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from exact_attention_49_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -38,9 +38,9 @@ _SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P] * 9 + [_I] * 6 + [_F, _I, _P, _S, _P]),
-    "fa_bwd_preprocess": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_main": (_I, [_P] * 7 + [_I] * 6 + [_F, _I, _P, _S, _P]),
-    "fa_bwd_postprocess": (_I, [_P, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_bwd_postprocess": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
     "fa_set_option": (_I, [ctypes.c_char_p, ctypes.c_double]),
     "fa_get_option": (_I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double)]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -114,8 +114,9 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dete
                         _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
-def fa_bwd_preprocess(o, do, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream=None) -> int:
-    return lib().fa_bwd_preprocess(_ptr(o), _ptr(do), B, H, Hkv, N, d, int(deterministic),
+def fa_bwd_preprocess(o, do, lse, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes,
+                      stream=None) -> int:
+    return lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), B, H, Hkv, N, d, int(deterministic),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
@@ -126,9 +127,9 @@ def fa_bwd_main(q, k, v, do, lse, dk, dv, B, H, Hkv, N, d, causal, scale, determ
                              _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
-def fa_bwd_postprocess(dq, B, H, Hkv, N, d, scale, deterministic, workspace, workspace_bytes,
+def fa_bwd_postprocess(dq, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes,
                        stream=None) -> int:
-    return lib().fa_bwd_postprocess(_ptr(dq), B, H, Hkv, N, d, float(scale), int(deterministic),
+    return lib().fa_bwd_postprocess(_ptr(dq), B, H, Hkv, N, d, int(deterministic),
                                     _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
@@ -199,6 +200,7 @@ def attention_backward(q, k, v, o, do, lse, causal: bool = False, scale: float |
     dv = torch.empty_like(v) if dv is None else dv
     ws_bytes = fa_bwd_workspace_bytes(B, H, Hkv, N, d, deterministic)
     if workspace is None:
+        # torch's caching allocator returns blocks aligned to at least 512 bytes
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     _check("fa_bwd", fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
                             deterministic, workspace, workspace.numel(), stream))

@@ -210,46 +210,131 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 
-size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic) {
-  if (check_shape(B, H, Hkv, N, d)) return 0;
+// Workspace layout: [dQ accumulator fp32 rows*d][(lse2, D) float2 rows][counters int32 B*H*N/128]
+struct BwdWorkspace {
+  size_t off_ld, off_cnt, total;
+};
+static BwdWorkspace bwd_ws_layout(int B, int H, int N, int d, int deterministic) {
   const size_t rows = (size_t)B * H * N;
-  size_t bytes = rows * d * 4 + rows * 4;  // dQ accumulator + D
-  bytes = (bytes + 255) & ~size_t(255);
-  if (deterministic) bytes += ((size_t)B * H * ((N + 127) / 128) * 4 + 255) & ~size_t(255);
-  return bytes;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  BwdWorkspace w;
+  w.off_ld = up(rows * d * 4);
+  w.off_cnt = up(w.off_ld + rows * 8);
+  w.total = w.off_cnt + (deterministic ? up((size_t)B * H * ((N + 127) / 128) * 4) : 0);
+  return w;
 }
 
-int fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int Hkv, int N, int d, int deterministic,
-                      void* workspace, size_t workspace_bytes, void* stream) {
-  (void)o; (void)dout; (void)B; (void)H; (void)Hkv; (void)N; (void)d; (void)deterministic;
-  (void)workspace; (void)workspace_bytes; (void)stream;
-  return FA_ERR_UNSUPPORTED;
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic) {
+  if (check_shape(B, H, Hkv, N, d)) return 0;
+  if (deterministic != 0 && deterministic != 1) return 0;
+  return bwd_ws_layout(B, H, N, d, deterministic).total;
+}
+
+// Checks shared by the three backward stages; returns FA_OK when there is work to launch,
+// 1 when the problem is empty (nothing to do), or an error status.
+static int check_bwd_common(int B, int H, int Hkv, int N, int d, int deterministic, const void* ws,
+                            size_t ws_bytes) {
+  int st = check_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  if (N % 128 != 0) return fail_detail(FA_ERR_UNSUPPORTED, "backward needs N % 128 == 0");
+  if (B == 0 || N == 0) return 1;
+  if (!ws) return FA_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return FA_ERR_MISALIGNED;
+  if (ws_bytes < bwd_ws_layout(B, H, N, d, deterministic).total) return FA_ERR_WORKSPACE;
+  return FA_OK;
+}
+
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int Hkv, int N, int d,
+                      int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_bwd_common(B, H, Hkv, N, d, deterministic, workspace, workspace_bytes);
+  if (st == 1) return FA_OK;
+  if (st) return st;
+  if (!o || !dout || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long rows = (long long)B * H * N;
+  cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float2*>(ws + w.off_ld),
+                                 reinterpret_cast<float*>(ws), deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr,
+                                 rows, (long long)B * H * (N / 128), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
 }
 
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse, void* dk, void* dv,
                 int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic, void* workspace,
                 size_t workspace_bytes, void* stream) {
-  (void)q; (void)k; (void)v; (void)dout; (void)lse; (void)dk; (void)dv; (void)B; (void)H; (void)Hkv; (void)N;
-  (void)d; (void)causal; (void)scale; (void)deterministic; (void)workspace; (void)workspace_bytes; (void)stream;
-  return FA_ERR_UNSUPPORTED;
+  (void)lse;  // the preprocess stage has staged LSE (in log2 units) into the workspace
+  int st = check_bwd_common(B, H, Hkv, N, d, deterministic, workspace, workspace_bytes);
+  if (st == 1) return FA_OK;
+  if (st) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (!q || !k || !v || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dk, 16) ||
+      !aligned(dv, 16))
+    return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_tmap_bf16_rows(&tq, q, d, N, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, N, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tv, v, d, N, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tdo, dout, d, N, (long long)B * H))
+    return FA_ERR_CUDA;
+  const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams p{};
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.ld = reinterpret_cast<const float2*>(ws + w.off_ld);
+  p.counters = deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.deterministic = deterministic;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale = scale;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_main launch", e);
 }
 
-int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, float scale, int deterministic,
-                       void* workspace, size_t workspace_bytes, void* stream) {
-  (void)dq; (void)B; (void)H; (void)Hkv; (void)N; (void)d; (void)scale; (void)deterministic; (void)workspace;
-  (void)workspace_bytes; (void)stream;
-  return FA_ERR_UNSUPPORTED;
+int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, int deterministic, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  int st = check_bwd_common(B, H, Hkv, N, d, deterministic, workspace, workspace_bytes);
+  if (st == 1) return FA_OK;
+  if (st) return st;
+  if (!dq) return FA_ERR_INVALID_ARG;
+  if (!aligned(dq, 16)) return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  cudaError_t e = launch_bwd_post(static_cast<const float*>(workspace), dq, (long long)B * H * N * d,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_postprocess launch", e);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
            void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
            void* workspace, size_t workspace_bytes, void* stream) {
-  int st = fa_bwd_preprocess(o, dout, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
+  // validate everything before the first launch
+  int st = check_bwd_common(B, H, Hkv, N, d, deterministic, workspace, workspace_bytes);
+  if (st == 1) return FA_OK;
+  if (st) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  st = fa_bwd_preprocess(o, dout, lse, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
   if (st) return st;
   st = fa_bwd_main(q, k, v, dout, lse, dk, dv, B, H, Hkv, N, d, causal, scale, deterministic, workspace,
                    workspace_bytes, stream);
   if (st) return st;
-  return fa_bwd_postprocess(dq, B, H, Hkv, N, d, scale, deterministic, workspace, workspace_bytes, stream);
+  return fa_bwd_postprocess(dq, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,518 @@
+// fa_bwd.cu -- exact attention backward for sm_103a.
+//
+// The backward recomputes P from the LSE saved by the forward instead of
+// storing it ("FlashAttention" wiki note, 定義 item (2); the explainer's
+// recomputation paragraph).  Three kernels:
+//
+//   preprocess   per query row: D = sum_c dO_c O_c (fp32) and LSE in log2 units,
+//                packed as (lse2, D); zero the fp32 dQ accumulator (and, in the
+//                deterministic mode, the ordering counters).
+//   main         one CTA per (b, K/V head g, 128-key tile j).  It keeps K_j, V_j in
+//                shared memory and dK, dV accumulators in tensor memory for the
+//                whole run, and walks every (query head of the group, 128-row
+//                query tile i) pair that can see the tile (causal: i >= j).  Per
+//                pair, five tcgen05 GEMMs (M = 128):
+//                  S^T  = K_j Q_i^T        (TMEM, fp32)
+//                  dP^T = V_j dO_i^T       (TMEM, fp32)
+//                  P^T  = exp2(S^T * scale*log2e - lse2_i)     (bf16, over S^T in TMEM)
+//                  dS^T = P^T * (dP^T - D_i) * scale           (bf16, over dP^T in TMEM
+//                                                               and in shared memory)
+//                  dV  += P^T dO_i,  dK += dS^T Q_i            (A operand from TMEM)
+//                  dQ_i = dS K_j                               (TMEM, then fp32
+//                                                               reductions into the
+//                                                               dQ accumulator)
+//                Grouped heads (GQA) share K_j/V_j, so dK/dV are summed over the
+//                group inside the CTA, in a fixed order, without atomics.
+//   postprocess  dQ accumulator (already scaled) -> bf16.
+//
+// The dQ accumulation over key tiles is the only cross-CTA sum.  Default: fp32
+// vector reductions (red.global.add.v4.f32) in whatever order CTAs reach them.
+// Deterministic mode (FA4's deterministic backward, wiki 未解決の問い): the CTA
+// of key tile j waits (bounded) until the tiles 0..j-1 have added their part of
+// query tile i, then adds with plain loads and stores, so the summation order is
+// fixed and results are bit-identical from run to run.
+//
+// Warp roles of the main kernel (512 threads, 16 warps):
+//   warps 0-3   compute, query columns 0-63 of each tile (thread = key row = TMEM lane)
+//   warps 4-7   compute, query columns 64-127
+//   warps 8-11  dQ read-out and reduction; at the end the dK/dV epilogue
+//   warp 12     MMA issuer (one thread) and TMEM allocator
+//   warp 13     TMA producer (one thread)
+//   warps 14-15 idle
+// Tensor memory (512 columns): dV | dK | S^T (later P^T) | dP^T (later dS^T, then dQ_i).
+#include <algorithm>
+
+#include "fa_internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128 * D * 2;  // one 128 x D bf16 tile
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;      // two stages
+  static constexpr int OFF_DO = 4 * TILE;     // two stages
+  static constexpr int OFF_DS = 6 * TILE;     // dS^T, 128 keys x 128 queries bf16, M-major, 128B swizzle
+  static constexpr int OFF_LD = OFF_DS + 32768;  // two stages of 128 x (lse2, D)
+  static constexpr int OFF_BAR = OFF_LD + 2048;
+  static constexpr int NBAR = 12;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr uint32_t COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+};
+
+FA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+FA_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+FA_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+FA_DEV void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+FA_DEV void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(512, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, -5);
+    return;
+  }
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t kv_full = bar0;
+  auto st_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  const uint32_t s_full = bar0 + 8u * 5, dp_full = bar0 + 8u * 6, p_ready = bar0 + 8u * 7;
+  const uint32_t ds_ready = bar0 + 8u * 8, dq_full = bar0 + 8u * 9, dq_empty = bar0 + 8u * 10;
+  const uint32_t mma_done = bar0 + 8u * 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // ---- work unit
+  const int N = p.N;
+  const int nq = N / 128;
+  const int BG = p.B * p.Hkv;
+  const int j = blockIdx.x / BG;
+  const int bg = blockIdx.x % BG;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int grp = p.H / p.Hkv;
+  const int i0 = p.causal ? j : 0;
+  const int ni = nq - i0;
+  const int ntiles = grp * ni;
+  auto tile_head = [&](int t) { return b * p.H + g * grp + t / ni; };  // b*H + h
+  auto tile_row = [&](int t) { return i0 + t % ni; };                 // query tile index i
+
+  if (warp == 0 && lane == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 13 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 13) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      for (int ch = 0; ch < C::CHUNKS; ++ch) {
+        tma_load_3d(sbase + C::OFF_K + ch * 16384, &tm_k, kv_full, ch * 64, j * 128, bg);
+        tma_load_3d(sbase + C::OFF_V + ch * 16384, &tm_v, kv_full, ch * 64, j * 128, bg);
+      }
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t & 1;
+        if (!mbar_wait(st_empty(s), ((t >> 1) & 1) ^ 1, abort, p.status)) break;
+        const int bh = tile_head(t), i = tile_row(t);
+        mbar_arrive_expect_tx(st_full(s), 2 * C::TILE + 1024);
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          tma_load_3d(sbase + C::OFF_Q + s * C::TILE + ch * 16384, &tm_q, st_full(s), ch * 64, i * 128, bh);
+          tma_load_3d(sbase + C::OFF_DO + s * C::TILE + ch * 16384, &tm_do, st_full(s), ch * 64, i * 128, bh);
+        }
+        bulk_load(sbase + C::OFF_LD + s * 1024, p.ld + ((size_t)bh * N + (size_t)i * 128), 1024, st_full(s));
+        issued = t + 1;
+      }
+      if (*abort) {  // let copies in flight land before the CTA exits (bounded)
+        for (int t = max(0, issued - 2); t < issued; ++t) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(st_full(t & 1), (t >> 1) & 1) && globaltimer() - t0 < 1000000ull) {
+          }
+        }
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(kv_full, 0) && globaltimer() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == 12) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);
+      auto ss_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t bsm) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bsm + off, 16, 1024), idS, kk > 0);
+        }
+      };
+      // D[128 keys x D] += A^T(TMEM, P^T or dS^T) * B(smem, M... [queries][D], MN-major)
+      auto ts_acc = [&](uint32_t dcol, uint32_t acol, uint32_t bsm, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + dcol, tmem + acol + 64 * (kk >> 2) + (kk & 3) * 8, sdesc_sw128(bsm + kk * 2048, 16384, 1024),
+                 idKV, (acc || kk > 0) ? 1u : 0u);
+      };
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+      auto sQ = [&](int s) { return sbase + C::OFF_Q + s * C::TILE; };
+      auto sDO = [&](int s) { return sbase + C::OFF_DO + s * C::TILE; };
+      bool ok = mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(st_full(0), 0, abort, p.status);
+      if (ok) {
+        tc_fence_after();
+        ss_kmajor(C::COL_S, sK, sQ(0));
+        mma_commit(s_full);
+        ss_kmajor(C::COL_DP, sV, sDO(0));
+        mma_commit(dp_full);
+      }
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t & 1;
+        const bool more = t + 1 < ntiles;
+        if (!(ok = mbar_wait(p_ready, t & 1, abort, p.status))) break;
+        tc_fence_after();
+        ts_acc(C::COL_DV, C::COL_S, sDO(s), t > 0);  // dV += P^T dO_t
+        if (more) {
+          if (!(ok = mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status))) break;
+          tc_fence_after();
+          ss_kmajor(C::COL_S, sK, sQ(s ^ 1));  // S^T of the next tile (P^T_t already consumed)
+          mma_commit(s_full);
+        }
+        if (!(ok = mbar_wait(ds_ready, t & 1, abort, p.status))) break;
+        tc_fence_after();
+        ts_acc(C::COL_DK, C::COL_DP, sQ(s), t > 0);  // dK += dS^T Q_t
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K_j, into the dP^T columns
+          mma_ss(tmem + C::COL_DP, sdesc_sw128(sDS + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
+                 idQ, kk > 0);
+        mma_commit(dq_full);
+        mma_commit(st_empty(s));
+        if (more) {
+          if (!(ok = mbar_wait(dq_empty, t & 1, abort, p.status))) break;
+          tc_fence_after();
+          ss_kmajor(C::COL_DP, sV, sDO(s ^ 1));
+          mma_commit(dp_full);
+        }
+      }
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, abort, p.status);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute: P^T and dS^T
+    const int w = warp >> 2;           // query-column half
+    const int r = threadIdx.x & 127;   // key row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::COL_S + 64 * w;
+    const uint32_t tDP = tmem + lane_off + C::COL_DP + 64 * w;
+    const float sl2 = p.scale_log2, scale = p.scale;
+    uint8_t* ds_row = smem + C::OFF_DS + w * 16384 + r * 128;
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t & 1;
+      const bool diag = p.causal && tile_row(t) == j;
+      const float4* ld4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024) + 32 * w;  // 2 queries per float4
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort, p.status))) break;
+      tc_fence_after();
+      float pv[64];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tS + 32 * cc, rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const float4 ld = ld4[16 * cc + c2];  // (lse2, D) of queries q, q+1
+          const int q = 64 * w + 32 * cc + 2 * c2;
+          float p0 = ex2_mufu(fmaf(__uint_as_float(rr[2 * c2]), sl2, -ld.x));
+          float p1 = ex2_mufu(fmaf(__uint_as_float(rr[2 * c2 + 1]), sl2, -ld.z));
+          if (diag) {
+            if (r > q) p0 = 0.f;
+            if (r > q + 1) p1 = 0.f;
+          }
+          pv[32 * cc + 2 * c2] = p0;
+          pv[32 * cc + 2 * c2 + 1] = p1;
+          pk[c2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + 16 * cc, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, abort, p.status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tDP + 32 * cc, rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const float4 ld = ld4[16 * cc + c2];
+          const float d0 = pv[32 * cc + 2 * c2] * (__uint_as_float(rr[2 * c2]) - ld.y) * scale;
+          const float d1 = pv[32 * cc + 2 * c2 + 1] * (__uint_as_float(rr[2 * c2 + 1]) - ld.w) * scale;
+          pk[c2] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tDP + 16 * cc, pk);
+        // dS^T row r, queries [32cc, 32cc+32) of this half: four 16-byte pieces, 128B-swizzled
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const int piece = 4 * cc + pc;
+          *reinterpret_cast<uint4*>(ds_row + ((piece ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2], pk[4 * pc + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dQ read-out, dK/dV epilogue
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tDQ = tmem + lane_off + C::COL_DP;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int bh = tile_head(t), i = tile_row(t);
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      float* dst = p.dq_acc + ((size_t)bh * N + (size_t)i * 128 + r) * D;
+      int* counter = p.deterministic ? p.counters + ((size_t)bh * nq + i) : nullptr;
+      if (p.deterministic) {
+        // wait for key tiles 0..j-1 to finish their part of this query tile
+        if (r == 0) {
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire(counter) != j) {
+            if (*abort || globaltimer() - t0 > kWaitLimitNs) {
+              *abort = 1;
+              atomicCAS(p.status, 0, kStatusTimeout);
+              break;
+            }
+          }
+        }
+        named_bar(1, 128);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDQ + 32 * c, v);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+        }
+        if (!p.deterministic) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            red_add_v4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                       __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+        } else if (!*abort) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * m);
+            float4 x = *a;
+            x.x += __uint_as_float(v[4 * m]);
+            x.y += __uint_as_float(v[4 * m + 1]);
+            x.z += __uint_as_float(v[4 * m + 2]);
+            x.w += __uint_as_float(v[4 * m + 3]);
+            *a = x;
+          }
+        }
+      }
+      if (p.deterministic) {
+        __threadfence();
+        named_bar(1, 128);
+        if (r == 0) st_release(counter, j + 1);
+      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (ntiles - 1) & 1, abort, p.status));
+    if (ok) {
+      // every MMA has completed (dq_full of the last tile is committed after all of them)
+      tc_fence_after();
+      const size_t krow = (size_t)bg * N + (size_t)j * 128 + r;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which ? p.dk : p.dv) + krow * D);
+        const uint32_t tcol = tmem + lane_off + (which ? C::COL_DK : C::COL_DV);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tcol + 32 * c, v);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            out[4 * c + m] =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]), __uint_as_float(v[8 * m + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 2]), __uint_as_float(v[8 * m + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 4]), __uint_as_float(v[8 * m + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 6]), __uint_as_float(v[8 * m + 7])));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- preprocess
+// One warp per query row: D = sum_c dO_c * O_c (fp32 products of bf16 inputs),
+// lse2 = LSE * log2(e).  Then zero the dQ accumulator and the counters.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                      const float* __restrict__ lse, float2* __restrict__ ld,
+                                                      float4* __restrict__ dq_acc, int* __restrict__ counters,
+                                                      long long rows, long long n_counters) {
+  constexpr int PER = D / 32;  // bf16 elements per lane
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  const long long gw = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long row = gw; row < rows; row += nwarps) {
+    const uint16_t* a = o + row * D + lane * PER;
+    const uint16_t* c = dout + row * D + lane * PER;
+    float acc = 0.f;
+    if (PER == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(a), y = *reinterpret_cast<const uint2*>(c);
+      const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
+        acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+      }
+    } else {
+      const uint32_t x = *reinterpret_cast<const uint32_t*>(a), y = *reinterpret_cast<const uint32_t*>(c);
+      acc = fmaf(__uint_as_float(x << 16), __uint_as_float(y << 16), acc);
+      acc = fmaf(__uint_as_float(x & 0xffff0000u), __uint_as_float(y & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) ld[row] = make_float2(lse[row] * 1.4426950408889634f, acc);
+  }
+  const long long n4 = rows * D / 4;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthr = (long long)gridDim.x * blockDim.x;
+  for (long long k = tid; k < n4; k += nthr) dq_acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (counters)
+    for (long long k = tid; k < n_counters; k += nthr) counters[k] = 0;
+}
+
+// ---------------------------------------------------------------- postprocess
+// dQ (bf16) = accumulator (fp32; the softmax scale is already folded into dS).
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4) {
+  const long long nthr = (long long)gridDim.x * blockDim.x;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += nthr) {
+    const float4 x = acc[k];
+    dq[k] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+  }
+}
+
+static int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
+}
+
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float2* ld, float* dq_acc,
+                           int* counters, long long rows, long long n_counters, cudaStream_t stream) {
+  const long long want = (rows + 7) / 8;
+  const int grid = (int)std::min<long long>(std::max<long long>(want, 1), (long long)sm_count() * 8);
+  if (d == 64)
+    bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                                 lse, ld, reinterpret_cast<float4*>(dq_acc), counters, rows, n_counters);
+  else
+    bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                                  lse, ld, reinterpret_cast<float4*>(dq_acc), counters, rows,
+                                                  n_counters);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream) {
+  const long long n4 = n / 4;
+  const int grid = (int)std::min<long long>(std::max<long long>((n4 + 255) / 256, 1), (long long)sm_count() * 8);
+  bwd_post_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const long long blocks = (long long)(p.N / 128) * p.B * p.Hkv;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  bwd_main_kernel<D><<<dim3((unsigned)blocks), dim3(512), C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_main_d<64>(tq, tk, tv, tdo, p, stream);
+  return launch_bwd_main_d<128>(tq, tk, tv, tdo, p, stream);
+}
+
+}  // namespace fa

@@ -214,10 +214,12 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tS = tmem + lane_off + (w ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_off + (w ? C::COL_O1 : C::COL_O0);
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;  // reference max (log2 units) of O and l
-    float l = 0.f;
+    float m_used = -INFINITY;      // reference max (log2 units) of O and l
+    uint64_t l_exact = 0;          // sum of p (fp32 pair): gives the LSE
+    uint64_t l_round = 0;          // sum of bf16(p), the weights the PV MMA used: normalises O
     bool ok = true;
     const int tile_row0 = q0 + w * 128;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     for (int j = 0; j < n_kv; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
       if (!ok) break;
@@ -238,9 +240,15 @@ __global__ void __launch_bounds__(320, 1)
           if ((p.causal && col > row) || col >= N) s[c] = -INFINITY;
         }
       }
-      float mx = s[0];
+      float mx4[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int a = 0; a < 4; ++a) {
+        float m = fmaxf(s[32 * a], s[32 * a + 1]);
+#pragma unroll
+        for (int c = 2; c < 32; c += 2) m = max3f(m, s[32 * a + c], s[32 * a + c + 1]);
+        mx4[a] = m;
+      }
+      const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
       const float m_tile = mx * sl2;
       const bool need = m_tile > m_used + p.tau;
       if (__any_sync(0xffffffffu, need)) {
@@ -261,19 +269,24 @@ __global__ void __launch_bounds__(320, 1)
           }
           tmem_st_wait();
         }
-        l *= alpha;
+        const uint64_t a2 = f2_pack(alpha, alpha);
+        l_exact = f2_mul(l_exact, a2);
+        l_round = f2_mul(l_round, a2);
         m_used = m_new;
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+      const uint64_t nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_mufu(fmaf(s[32 * c + 2 * i], sl2, neg_m));
-          const float p1 = ex2_mufu(fmaf(s[32 * c + 2 * i + 1], sl2, neg_m));
-          l += p0 + p1;
+          const float2 x = f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nm2));
+          const float p0 = ex2_mufu(x.x);
+          const float p1 = ex2_mufu(x.y);
           pk[i] = pack_bf16x2(p0, p1);
+          l_exact = f2_add(l_exact, f2_pack(p0, p1));
+          l_round = f2_add(l_round, bf16x2_widen(pk[i]));
         }
         tmem_st16(tS + 16 * c, pk);
       }
@@ -285,7 +298,9 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (n_kv - 1) & 1, abort, p.status));
     if (ok) {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float2 le = f2_unpack(l_exact), lr = f2_unpack(l_round);
+      const float l = le.x + le.y, lrs = lr.x + lr.y;
+      const float inv_l = lrs > 0.f ? 1.f / lrs : 0.f;
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * N + row) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

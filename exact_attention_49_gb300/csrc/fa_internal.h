@@ -26,6 +26,26 @@ struct FwdParams {
   int* status;       // device status word
 };
 
+struct BwdParams {
+  void* dk;           // bf16 [B,Hkv,N,d]
+  void* dv;           // bf16 [B,Hkv,N,d]
+  float* dq_acc;      // fp32 [B,H,N,d] dQ accumulator (workspace)
+  const float2* ld;   // per query row (LSE * log2 e, D) (workspace)
+  int* counters;      // deterministic mode: [B*H*(N/128)] ordering counters (workspace)
+  int B, H, Hkv, N;
+  int causal;
+  int deterministic;
+  float scale_log2;   // softmax scale * log2(e)
+  float scale;        // softmax scale (folded into dS)
+  int* status;        // device status word
+};
+
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float2* ld, float* dq_acc,
+                           int* counters, long long rows, long long n_counters, cudaStream_t stream);
+cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream);
+
 // Launch the forward kernel for head dim d (64 or 128).  Returns a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t stream);

@@ -70,8 +70,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
 
 /* Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
- * [B,H,N,d], the fp32 row terms D [B,H,N], and (deterministic mode) one
- * int32 ordering counter per (b, h, 128-row query block).  0 on bad sizes. */
+ * [B,H,N,d], one (LSE in log2 units, D) fp32 pair per query row, and
+ * (deterministic mode) one int32 ordering counter per (b, h, 128-row query
+ * block).  The workspace must be 256-byte aligned.  0 on bad sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic);
 
 /* Backward: dq, dk, dv (bf16) from q, k, v, o, dout (bf16) and lse (fp32, as
@@ -85,16 +86,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of fa_bwd, exposed so that callers (and the benchmark) can
- * time or schedule them separately.  Same arguments and checks as fa_bwd.
- *   preprocess : D_i = sum_c dO_ic O_ic (fp32), zero the dQ accumulator and counters
- *   main       : recompute P from LSE tile by tile; dK, dV written; dQ accumulated
- *   postprocess: dQ = scale * accumulator, rounded to bf16 */
-int fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int Hkv, int N, int d,
-                      int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+ * time or schedule them separately; they must run in this order on one
+ * stream with the same workspace.  Same argument checks as fa_bwd.
+ *   preprocess : D_i = sum_c dO_ic O_ic (fp32) and LSE_i * log2(e) into the
+ *                workspace; zero the dQ accumulator (and counters)
+ *   main       : recompute P from LSE tile by tile; write dK, dV; accumulate
+ *                scale * dS K into the dQ accumulator.  `lse` is accepted for
+ *                symmetry and not read (preprocess staged it).
+ *   postprocess: dQ = accumulator rounded to bf16 */
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int Hkv, int N,
+                      int d, int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
                 void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
                 int deterministic, void* workspace, size_t workspace_bytes, void* stream);
-int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, float scale,
+int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d,
                        int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Ablation switches (process-wide; take effect on the next call):

@@ -95,3 +95,21 @@ def test_workspace_size(L):
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, d, 1) > ws
     assert fa.fa_bwd_workspace_bytes(B, 3, 2, N, d, 0) == 0
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 96, 0) == 0
+
+
+def test_bwd_validation(L):
+    from exact_attention_49_gb300 import binding as fa
+    def bwd(q=GOOD, B=1, H=2, Hkv=1, N=256, d=64, causal=0, scale=0.125, det=0, ws=GOOD, wsb=1 << 30):
+        return L.fa_bwd(q, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, B, H, Hkv, N, d, causal, scale, det,
+                        ws, wsb, None)
+    assert bwd(q=None) == fa.FA_ERR_INVALID_ARG
+    assert bwd(H=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
+    assert bwd(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(N=200) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(ws=None) == fa.FA_ERR_WORKSPACE
+    assert bwd(wsb=1024) == fa.FA_ERR_WORKSPACE
+    assert bwd(ws=P((1 << 20) + 16)) == fa.FA_ERR_MISALIGNED
+    assert bwd(q=BAD) == fa.FA_ERR_MISALIGNED
+    assert bwd(det=2) == fa.FA_ERR_INVALID_ARG
+    assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(N=0, q=None, ws=None) == fa.FA_OK

@@ -1,0 +1,130 @@
+"""GPU parity of fa_bwd against the fp64 CPU oracle's analytic backward.
+
+The GPU backward consumes the GPU forward's O and LSE (as a training step
+would); the oracle computes the gradients of sum(O * dO) from Q, K, V, dO
+alone.  Small cases are compared on every element; the full-size workloads run
+on the GPU at full size and are compared on sampled query heads (dQ) and on the
+K/V heads they belong to (dK, dV summed over the whole group).  The
+deterministic mode is also checked for bit-identical results across runs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_49_gb300 import binding as fa
+from exact_attention_49_gb300.inputs import WORKLOADS, make_inputs
+from oracle import reference as ref
+from parity import GRAD_RTOL, rel_fro, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_attention_49_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+
+
+def gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic=False):
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, dod, lse, causal=causal, scale=scale,
+                                       deterministic=deterministic)
+    torch.cuda.synchronize()
+    st = fa.fa_last_device_status()
+    assert st == fa.FA_OK, fa.status_string(st)
+    return dq, dk, dv
+
+
+def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0, deterministic=False):
+    q, k, v, do = make_inputs(B, H, Hkv, N, d, seed, qk_mult)
+    scale = d ** -0.5
+    dq, dk, dv = gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic)
+    rq, rk, rv = ref.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, scale)
+    errs = (rel_fro(to64(dq), rq), rel_fro(to64(dk), rk), rel_fro(to64(dv), rv))
+    assert max(errs) <= GRAD_RTOL, errs
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [128, 256, 640])
+def test_bwd_small(N, causal, d):
+    check_full(1, 2, 2, N, d, causal, seed=200 + N + d)
+
+
+def test_bwd_c1():
+    w = WORKLOADS["C1"]
+    check_full(w.B, w.H, w.Hkv, w.N, w.d, w.causal, w.seed)
+
+
+def test_bwd_c2():
+    w = WORKLOADS["C2"]
+    check_full(w.B, w.H, w.Hkv, w.N, w.d, w.causal, w.seed)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("det", [False, True])
+def test_bwd_gqa_small(causal, d, det):
+    check_full(2, 8, 2, 512, d, causal, seed=17, deterministic=det)
+
+
+def test_bwd_stress_rescale_inputs():
+    check_full(1, 4, 4, 1024, 128, True, seed=19, qk_mult=4.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_deterministic_bit_identical(causal):
+    B, H, Hkv, N, d = 2, 8, 2, 1024, 128
+    q, k, v, do = make_inputs(B, H, Hkv, N, d, seed=23)
+    scale = d ** -0.5
+    first = gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic=True)
+    for _ in range(2):
+        again = gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic=True)
+        for a, b in zip(first, again):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_bwd_workspace_checks():
+    B, H, Hkv, N, d = 1, 2, 2, 256, 64
+    q, k, v, do = (t.cuda() for t in make_inputs(B, H, Hkv, N, d, seed=1))
+    o, lse = fa.attention_forward(q, k, v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, d, 0, d ** -0.5, 0)
+    assert fa.fa_bwd(*args, ws, need - 256) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd(*args, None, need) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd(*args, ws, need) == fa.FA_OK
+    bad = (q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, 200, d, 0, d ** -0.5, 0)
+    assert fa.fa_bwd(*bad, ws, need) == fa.FA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+
+
+def _sample_heads(B, H, seed, n=4):
+    rng = np.random.default_rng(seed)
+    pick = {(0, 0), (B - 1, H - 1)}
+    while len(pick) < min(n, B * H):
+        pick.add((int(rng.integers(B)), int(rng.integers(H))))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name,det", [("C3", False), ("C3b", False), ("C4", False), ("C4", True)])
+def test_bwd_full_size_sampled(name, det):
+    w = WORKLOADS[name]
+    q, k, v, do = make_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.seed, w.qk_mult)
+    dq, dk, dv = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, deterministic=det)
+    grp = w.H // w.Hkv
+    # whole K/V groups around sampled query heads: (0,0), (B-1,H-1) and, for
+    # single-head groups, two seeded-random heads (GQA groups are 4x the oracle work)
+    groups = sorted({(b, h // grp) for b, h in _sample_heads(w.B, w.H, w.seed, n=4 if grp == 1 else 2)})
+    for b, g in groups:
+        hs = slice(g * grp, (g + 1) * grp)
+        rq, rk, rv = ref.attn_bwd(to64(q[b:b + 1, hs]), to64(k[b:b + 1, g:g + 1]), to64(v[b:b + 1, g:g + 1]),
+                                  to64(do[b:b + 1, hs]), w.causal, w.scale)
+        errs = (rel_fro(to64(dq[b:b + 1, hs]), rq), rel_fro(to64(dk[b:b + 1, g:g + 1]), rk),
+                rel_fro(to64(dv[b:b + 1, g:g + 1]), rv))
+        assert max(errs) <= GRAD_RTOL, ((b, g), errs)
