@@ -102,6 +102,34 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
 int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d,
                        int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the scratch array that fa_bwd_noalloc uses (32 MiB per device). */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* fa_bwd_noalloc -- the backward for callers that cannot allocate device
+ * memory.  (The paper has no counterpart: this is a convenience of this
+ * library.)  fa_bwd needs a caller-allocated workspace; some callers have no
+ * allocator at the call site -- e.g. a plugin or operator run by a host
+ * framework that owns all device memory and hands out no scratch, or code on a
+ * latency-critical path where cudaMalloc is not allowed because it can
+ * synchronise the device.  This entry point takes the same inputs and outputs
+ * as fa_bwd (the caller still owns q, k, v, o, dout, lse, dq, dk, dv) but uses
+ * a fixed, library-owned device array of FA_NOALLOC_SCRATCH_BYTES as its
+ * workspace, and allocates nothing.
+ *   - A problem with fa_bwd_workspace_bytes(...) > FA_NOALLOC_SCRATCH_BYTES is
+ *     rejected with FA_ERR_WORKSPACE before anything runs.
+ *   - Each device that loads the library holds the array until process exit.
+ *   - All calls share the array; it keeps the last call's contents, and the
+ *     call itself clears what must start at zero.  Calls that may overlap on
+ *     the GPU (several streams or host threads on one device) race on it:
+ *     serialise them on one stream.
+ *   - The first call on a device looks up the array's device address and
+ *     caches it; make that first call before any stream capture.
+ * Other arguments, checks and status codes are those of fa_bwd. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
+                   void* stream);
+
 /* Ablation switches (process-wide; take effect on the next call):
  *   "rescale_threshold"  tau >= 0 in log2 units (default 8): the running-max
  *                        correction of O and l is skipped unless the row max
