@@ -384,11 +384,15 @@ def main():
     ap.add_argument("--workload", default="C3")
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling on a smaller case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from exact_attention_49_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=w.name.replace("B%d " % w.B, "B%d " % args.batch))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -61,6 +61,8 @@ struct BwdCfg {
   static constexpr int NBAR = 12;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+  // d = 128: dQ is produced transposed (TMEM lane = head-dim column) for coalesced reductions
+  static constexpr bool DQ_T = (D == 128);
 };
 
 FA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -71,6 +73,9 @@ FA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
 FA_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+FA_DEV void red_add(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
 FA_DEV int ld_acquire(const int* p) {
   int v;
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);
+      constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);
       auto ss_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t bsm) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -229,10 +235,19 @@ __global__ void __launch_bounds__(512, 1)
         if (!(ok = mbar_wait(ds_ready, t & 1, abort, p.status))) break;
         tc_fence_after();
         ts_acc(C::COL_DK, C::COL_DP, sQ(s), t > 0);  // dK += dS^T Q_t
+        if constexpr (C::DQ_T) {
+          // dQ_t^T = K_j^T dS^T (M = d, N = queries) into the dP^T columns: TMEM lane = head-dim
+          // column, so the read-out warps reduce 128 contiguous bytes per instruction
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K_j, into the dP^T columns
-          mma_ss(tmem + C::COL_DP, sdesc_sw128(sDS + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
-                 idQ, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::COL_DP, sdesc_sw128(sK + kk * 2048, 16384, 1024),
+                   sdesc_sw128(sDS + kk * 2048, 16384, 1024), idQT, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K_j, into the dP^T columns
+            mma_ss(tmem + C::COL_DP, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
+                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idQ, kk > 0);
+        }
         mma_commit(dq_full);
         mma_commit(st_empty(s));
         if (more) {
@@ -325,7 +340,6 @@ __global__ void __launch_bounds__(512, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort, p.status));
       if (!ok) break;
       tc_fence_after();
-      float* dst = p.dq_acc + ((size_t)bh * N + (size_t)i * 128 + r) * D;
       int* counter = p.deterministic ? p.counters + ((size_t)bh * nq + i) : nullptr;
       if (p.deterministic) {
         // wait for key tiles 0..j-1 to finish their part of this query tile
@@ -341,29 +355,51 @@ __global__ void __launch_bounds__(512, 1)
         }
         named_bar(1, 128);
       }
+      if constexpr (C::DQ_T) {
+        // thread r holds column r of dQ_i: rows q = 32c .. 32c+31 per TMEM load
+        float* col = p.dq_acc + ((size_t)bh * N + (size_t)i * 128) * D + r;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDQ + 32 * c, v);
-        if (c == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(dq_empty);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tDQ + 32 * c, v);
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
+          if (!p.deterministic) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) red_add(col + (size_t)(32 * c + m) * D, __uint_as_float(v[m]));
+          } else if (!*abort) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) col[(size_t)(32 * c + m) * D] += __uint_as_float(v[m]);
+          }
         }
-        if (!p.deterministic) {
+      } else {
+        float* dst = p.dq_acc + ((size_t)bh * N + (size_t)i * 128 + r) * D;
 #pragma unroll
-          for (int m = 0; m < 8; ++m)
-            red_add_v4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                       __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
-        } else if (!*abort) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tDQ + 32 * c, v);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
+          if (!p.deterministic) {
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * m);
-            float4 x = *a;
-            x.x += __uint_as_float(v[4 * m]);
-            x.y += __uint_as_float(v[4 * m + 1]);
-            x.z += __uint_as_float(v[4 * m + 2]);
-            x.w += __uint_as_float(v[4 * m + 3]);
-            *a = x;
+            for (int m = 0; m < 8; ++m)
+              red_add_v4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                         __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+          } else if (!*abort) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * m);
+              float4 x = *a;
+              x.x += __uint_as_float(v[4 * m]);
+              x.y += __uint_as_float(v[4 * m + 1]);
+              x.z += __uint_as_float(v[4 * m + 2]);
+              x.w += __uint_as_float(v[4 * m + 3]);
+              *a = x;
+            }
           }
         }
       }
