@@ -210,16 +210,17 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 
-// Workspace layout: [dQ accumulator fp32 rows*d][(lse2, D) float2 rows][counters int32 B*H*N/128]
+// Workspace layout: [dQ accumulator fp32 rows*d][lse2 fp32 rows][D fp32 rows][counters int32 B*H*N/128]
 struct BwdWorkspace {
-  size_t off_ld, off_cnt, total;
+  size_t off_lse2, off_d, off_cnt, total;
 };
 static BwdWorkspace bwd_ws_layout(int B, int H, int N, int d, int deterministic) {
   const size_t rows = (size_t)B * H * N;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdWorkspace w;
-  w.off_ld = up(rows * d * 4);
-  w.off_cnt = up(w.off_ld + rows * 8);
+  w.off_lse2 = up(rows * d * 4);
+  w.off_d = up(w.off_lse2 + rows * 4);
+  w.off_cnt = up(w.off_d + rows * 4);
   w.total = w.off_cnt + (deterministic ? up((size_t)B * H * ((N + 127) / 128) * 4) : 0);
   return w;
 }
@@ -256,8 +257,9 @@ int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, 
   const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * N;
-  cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float2*>(ws + w.off_ld),
-                                 reinterpret_cast<float*>(ws), deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr,
+  cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float*>(ws + w.off_lse2),
+                                 reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws),
+                                 deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr,
                                  rows, (long long)B * H * (N / 128), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
 }
@@ -287,7 +289,8 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
   p.dk = dk;
   p.dv = dv;
   p.dq_acc = reinterpret_cast<float*>(ws);
-  p.ld = reinterpret_cast<const float2*>(ws + w.off_ld);
+  p.lse2 = reinterpret_cast<const float*>(ws + w.off_lse2);
+  p.dvec = reinterpret_cast<const float*>(ws + w.off_d);
   p.counters = deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr;
   p.B = B;
   p.H = H;

@@ -4,8 +4,8 @@
 // storing it ("FlashAttention" wiki note, 定義 item (2); the explainer's
 // recomputation paragraph).  Three kernels:
 //
-//   preprocess   per query row: D = sum_c dO_c O_c (fp32) and LSE in log2 units,
-//                packed as (lse2, D); zero the fp32 dQ accumulator (and, in the
+//   preprocess   per query row: D = sum_c dO_c O_c (fp32) and LSE in log2 units
+//                (two fp32 arrays); zero the fp32 dQ accumulator (and, in the
 //                deterministic mode, the ordering counters).
 //   main         one CTA per (b, K/V head g, 128-key tile j).  It keeps K_j, V_j in
 //                shared memory and dK, dV accumulators in tensor memory for the
@@ -56,7 +56,7 @@ struct BwdCfg {
   static constexpr int OFF_Q = 2 * TILE;      // two stages
   static constexpr int OFF_DO = 4 * TILE;     // two stages
   static constexpr int OFF_DS = 6 * TILE;     // dS^T, 128 keys x 128 queries bf16, M-major, 128B swizzle
-  static constexpr int OFF_LD = OFF_DS + 32768;  // two stages of 128 x (lse2, D)
+  static constexpr int OFF_LD = OFF_DS + 32768;  // two stages of lse2[128] then D[128] (fp32)
   static constexpr int OFF_BAR = OFF_LD + 2048;
   static constexpr int NBAR = 12;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
@@ -174,7 +174,9 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_3d(sbase + C::OFF_Q + s * C::TILE + ch * 16384, &tm_q, st_full(s), ch * 64, i * 128, bh);
           tma_load_3d(sbase + C::OFF_DO + s * C::TILE + ch * 16384, &tm_do, st_full(s), ch * 64, i * 128, bh);
         }
-        bulk_load(sbase + C::OFF_LD + s * 1024, p.ld + ((size_t)bh * N + (size_t)i * 128), 1024, st_full(s));
+        const size_t row0 = (size_t)bh * N + (size_t)i * 128;
+        bulk_load(sbase + C::OFF_LD + s * 1024, p.lse2 + row0, 512, st_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 1024 + 512, p.dvec + row0, 512, st_full(s));
         issued = t + 1;
       }
       if (*abort) {  // let copies in flight land before the CTA exits (bounded)
@@ -267,34 +269,49 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::COL_S + 64 * w;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + 64 * w;
-    const float sl2 = p.scale_log2, scale = p.scale;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t scx2 = f2_pack(p.scale, p.scale);
     uint8_t* ds_row = smem + C::OFF_DS + w * 16384 + r * 128;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
       const bool diag = p.causal && tile_row(t) == j;
-      const float4* ld4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024) + 32 * w;  // 2 queries per float4
+      // this half's 64 queries: lse2 and D, four per 16-byte shared load
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024) + 16 * w;
+      const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024 + 512) + 16 * w;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort, p.status))) break;
       tc_fence_after();
       float pv[64];
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nowait(tS, ra);
+        tmem_ld32_nowait(tS + 32, rb);
+        tmem_wait_ld(ra);
+        tmem_wait_ld(rb);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 L = lse4[c4];
+          const uint32_t* src = (c4 < 8) ? ra : rb;
+          const int o = (c4 & 7) * 4;
+          const float2 x01 = f2_unpack(f2_fma(f2_pack(__uint_as_float(src[o]), __uint_as_float(src[o + 1])), sl2x2,
+                                              f2_pack(-L.x, -L.y)));
+          const float2 x23 = f2_unpack(f2_fma(f2_pack(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3])), sl2x2,
+                                              f2_pack(-L.z, -L.w)));
+          pv[4 * c4] = ex2_mufu(x01.x);
+          pv[4 * c4 + 1] = ex2_mufu(x01.y);
+          pv[4 * c4 + 2] = ex2_mufu(x23.x);
+          pv[4 * c4 + 3] = ex2_mufu(x23.y);
+        }
+      }
+      if (diag) {  // key r > query q is masked on the diagonal tile
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (r > 64 * w + c) pv[c] = 0.f;
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(tS + 32 * cc, rr);
         uint32_t pk[16];
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const float4 ld = ld4[16 * cc + c2];  // (lse2, D) of queries q, q+1
-          const int q = 64 * w + 32 * cc + 2 * c2;
-          float p0 = ex2_mufu(fmaf(__uint_as_float(rr[2 * c2]), sl2, -ld.x));
-          float p1 = ex2_mufu(fmaf(__uint_as_float(rr[2 * c2 + 1]), sl2, -ld.z));
-          if (diag) {
-            if (r > q) p0 = 0.f;
-            if (r > q + 1) p1 = 0.f;
-          }
-          pv[32 * cc + 2 * c2] = p0;
-          pv[32 * cc + 2 * c2 + 1] = p1;
-          pk[c2] = pack_bf16x2(p0, p1);
-        }
+        for (int c2 = 0; c2 < 16; ++c2) pk[c2] = pack_bf16x2(pv[32 * cc + 2 * c2], pv[32 * cc + 2 * c2 + 1]);
         tmem_st16(tS + 16 * cc, pk);
       }
       tmem_st_wait();
@@ -303,25 +320,37 @@ __global__ void __launch_bounds__(512, 1)
 
       if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, abort, p.status))) break;
       tc_fence_after();
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nowait(tDP, ra);
+        tmem_ld32_nowait(tDP + 32, rb);
+        tmem_wait_ld(ra);
+        tmem_wait_ld(rb);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(tDP + 32 * cc, rr);
-        uint32_t pk[16];
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t* src = cc ? rb : ra;
+          uint32_t pk[16];
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const float4 ld = ld4[16 * cc + c2];
-          const float d0 = pv[32 * cc + 2 * c2] * (__uint_as_float(rr[2 * c2]) - ld.y) * scale;
-          const float d1 = pv[32 * cc + 2 * c2 + 1] * (__uint_as_float(rr[2 * c2 + 1]) - ld.w) * scale;
-          pk[c2] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(tDP + 16 * cc, pk);
-        // dS^T row r, queries [32cc, 32cc+32) of this half: four 16-byte pieces, 128B-swizzled
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 Dv = d4[8 * cc + c4];
+            const int o = 4 * c4, q = 32 * cc + 4 * c4;
+            // dS = P * (dP - D) * scale, two columns per packed op
+            const uint64_t a = f2_add(f2_pack(__uint_as_float(src[o]), __uint_as_float(src[o + 1])), f2_pack(-Dv.x, -Dv.y));
+            const uint64_t b = f2_add(f2_pack(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3])),
+                                      f2_pack(-Dv.z, -Dv.w));
+            const float2 d01 = f2_unpack(f2_mul(f2_mul(a, f2_pack(pv[q], pv[q + 1])), scx2));
+            const float2 d23 = f2_unpack(f2_mul(f2_mul(b, f2_pack(pv[q + 2], pv[q + 3])), scx2));
+            pk[2 * c4] = pack_bf16x2(d01.x, d01.y);
+            pk[2 * c4 + 1] = pack_bf16x2(d23.x, d23.y);
+          }
+          tmem_st16(tDP + 16 * cc, pk);
+          // dS^T row r, queries [32cc, 32cc+32) of this half: four 16-byte pieces, 128B-swizzled
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const int piece = 4 * cc + pc;
-          *reinterpret_cast<uint4*>(ds_row + ((piece ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2], pk[4 * pc + 3]);
+          for (int pc = 0; pc < 4; ++pc) {
+            const int piece = 4 * cc + pc;
+            *reinterpret_cast<uint4*>(ds_row + ((piece ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2], pk[4 * pc + 3]);
+          }
         }
       }
       tmem_st_wait();
@@ -356,22 +385,31 @@ __global__ void __launch_bounds__(512, 1)
         named_bar(1, 128);
       }
       if constexpr (C::DQ_T) {
-        // thread r holds column r of dQ_i: rows q = 32c .. 32c+31 per TMEM load
+        // thread r holds column r of dQ_i (rows q = 0..127).  Read rows 0-63, reduce
+        // them, read rows 64-127, hand the TMEM columns back to the MMA warp, reduce.
         float* col = p.dq_acc + ((size_t)bh * N + (size_t)i * 128) * D + r;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tDQ + 32 * c, v);
-          if (c == 3) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t va[32], vb[32];
+          tmem_ld32_nowait(tDQ + 64 * half, va);
+          tmem_ld32_nowait(tDQ + 64 * half + 32, vb);
+          tmem_wait_ld(va);
+          tmem_wait_ld(vb);
+          if (half == 1) {
             tc_fence_before();
             mbar_arrive(dq_empty);
           }
+          float* c0 = col + (size_t)(64 * half) * D;
           if (!p.deterministic) {
 #pragma unroll
-            for (int m = 0; m < 32; ++m) red_add(col + (size_t)(32 * c + m) * D, __uint_as_float(v[m]));
+            for (int m = 0; m < 32; ++m) red_add(c0 + (size_t)m * D, __uint_as_float(va[m]));
+#pragma unroll
+            for (int m = 0; m < 32; ++m) red_add(c0 + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
           } else if (!*abort) {
 #pragma unroll
-            for (int m = 0; m < 32; ++m) col[(size_t)(32 * c + m) * D] += __uint_as_float(v[m]);
+            for (int m = 0; m < 32; ++m) c0[(size_t)m * D] += __uint_as_float(va[m]);
+#pragma unroll
+            for (int m = 0; m < 32; ++m) c0[(size_t)(32 + m) * D] += __uint_as_float(vb[m]);
           }
         }
       } else {
@@ -447,7 +485,8 @@ __global__ void __launch_bounds__(512, 1)
 // lse2 = LSE * log2(e).  Then zero the dQ accumulator and the counters.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                      const float* __restrict__ lse, float2* __restrict__ ld,
+                                                      const float* __restrict__ lse, float* __restrict__ lse2,
+                                                      float* __restrict__ dvec,
                                                       float4* __restrict__ dq_acc, int* __restrict__ counters,
                                                       long long rows, long long n_counters) {
   constexpr int PER = D / 32;  // bf16 elements per lane
@@ -473,7 +512,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) ld[row] = make_float2(lse[row] * 1.4426950408889634f, acc);
+    if (lane == 0) {
+      lse2[row] = lse[row] * 1.4426950408889634f;
+      dvec[row] = acc;
+    }
   }
   const long long n4 = rows * D / 4;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -505,16 +547,17 @@ static int sm_count() {
   return n[dev];
 }
 
-cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float2* ld, float* dq_acc,
-                           int* counters, long long rows, long long n_counters, cudaStream_t stream) {
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
+                           float* dq_acc, int* counters, long long rows, long long n_counters, cudaStream_t stream) {
   const long long want = (rows + 7) / 8;
   const int grid = (int)std::min<long long>(std::max<long long>(want, 1), (long long)sm_count() * 8);
   if (d == 64)
     bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                                 lse, ld, reinterpret_cast<float4*>(dq_acc), counters, rows, n_counters);
+                                                 lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, rows,
+                                                 n_counters);
   else
     bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                                  lse, ld, reinterpret_cast<float4*>(dq_acc), counters, rows,
+                                                  lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, rows,
                                                   n_counters);
   return cudaGetLastError();
 }

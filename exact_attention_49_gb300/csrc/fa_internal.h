@@ -30,7 +30,8 @@ struct BwdParams {
   void* dk;           // bf16 [B,Hkv,N,d]
   void* dv;           // bf16 [B,Hkv,N,d]
   float* dq_acc;      // fp32 [B,H,N,d] dQ accumulator (workspace)
-  const float2* ld;   // per query row (LSE * log2 e, D) (workspace)
+  const float* lse2;  // per query row LSE * log2(e) (workspace)
+  const float* dvec;  // per query row D = sum_c dO_c O_c (workspace)
   int* counters;      // deterministic mode: [B*H*(N/128)] ordering counters (workspace)
   int B, H, Hkv, N;
   int causal;
@@ -40,8 +41,8 @@ struct BwdParams {
   int* status;        // device status word
 };
 
-cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float2* ld, float* dq_acc,
-                           int* counters, long long rows, long long n_counters, cudaStream_t stream);
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
+                           float* dq_acc, int* counters, long long rows, long long n_counters, cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream);
