@@ -115,8 +115,17 @@ __global__ void __launch_bounds__(512, 1)
   const int N = p.N;
   const int nq = N / 128;
   const int BG = p.B * p.Hkv;
-  const int j = blockIdx.x / BG;
-  const int bg = blockIdx.x % BG;
+  // CTA order: groups of (up to) 8 K/V heads, key tiles heaviest first (j = 0) within a
+  // group.  The CTAs resident at any time then share few heads' Q/dO tiles and dQ
+  // accumulator lines, which stay in L2 (about 14% faster than key-tile-major order
+  // over all heads on the B4 H16 N8192 workload).
+  constexpr int kHeadGroup = 8;
+  const int nkv = N / 128;
+  const int gi = blockIdx.x / (kHeadGroup * nkv);
+  const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
+  const int rem = blockIdx.x - gi * kHeadGroup * nkv;
+  const int j = rem / gsz;
+  const int bg = gi * kHeadGroup + rem % gsz;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int grp = p.H / p.Hkv;
   const int i0 = p.causal ? j : 0;
