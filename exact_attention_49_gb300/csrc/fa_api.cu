@@ -145,7 +145,8 @@ int fa_set_option(const char* key, double value) {
     return FA_OK;
   }
   if (!std::strcmp(key, "poly_exp")) {
-    if (value != std::floor(value) || value < -1.0 || value > 32.0) return FA_ERR_INVALID_ARG;
+    if (value != -1.0 && value != 0.0 && value != 4.0 && value != 8.0 && value != 12.0 && value != 16.0)
+      return FA_ERR_INVALID_ARG;
     options().poly_exp = static_cast<int>(value);
     return FA_OK;
   }
@@ -206,7 +207,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.tau = options().rescale_threshold;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 

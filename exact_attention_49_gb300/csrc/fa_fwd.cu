@@ -43,7 +43,9 @@ struct FwdCfg {
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
 };
 
-template <int D>
+// POLY: how many of every 16 column pairs take the FMA-pipe polynomial exp2 instead of
+// the MUFU ex2 unit (0 = MUFU only).
+template <int D, int POLY>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -281,9 +283,17 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nm2));
-          const float p0 = ex2_mufu(x.x);
-          const float p1 = ex2_mufu(x.y);
+          const uint64_t x2 = f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nm2);
+          float p0, p1;
+          if ((i * POLY) % 16 < POLY) {
+            const float2 pp = f2_unpack(ex2_poly2(x2));
+            p0 = pp.x;
+            p1 = pp.y;
+          } else {
+            const float2 x = f2_unpack(x2);
+            p0 = ex2_mufu(x.x);
+            p1 = ex2_mufu(x.y);
+          }
           pk[i] = pack_bf16x2(p0, p1);
           l_exact = f2_add(l_exact, f2_pack(p0, p1));
           l_round = f2_add(l_round, bf16x2_widen(pk[i]));
@@ -328,29 +338,42 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D>
-static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdParams& p, cudaStream_t stream) {
+template <int D, int POLY>
+static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   const long long blocks = (long long)((p.N + 255) / 256) * p.B * p.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  fwd_kernel<D><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  fwd_kernel<D, POLY><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdParams& p, int poly_cols, cudaStream_t stream) {
+  switch (poly_cols) {  // columns of every 32 on the polynomial
+    case 0: return launch_fwd_dp<D, 0>(tq, tk, tv, p, stream);
+    case 4: return launch_fwd_dp<D, 2>(tq, tk, tv, p, stream);
+    case 8: return launch_fwd_dp<D, 4>(tq, tk, tv, p, stream);
+    case 12: return launch_fwd_dp<D, 6>(tq, tk, tv, p, stream);
+    case 16: return launch_fwd_dp<D, 8>(tq, tk, tv, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, cudaStream_t stream) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, stream);
-  return launch_fwd_d<128>(tq, tk, tv, p, stream);
+                       const FwdParams& p, int poly_cols, cudaStream_t stream) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, poly_cols, stream);
+  return launch_fwd_d<128>(tq, tk, tv, p, poly_cols, stream);
 }
 
 }  // namespace fa

@@ -11,7 +11,7 @@ namespace fa {
 // Runtime-tunable switches (set through fa_set_option).
 struct Options {
   float rescale_threshold = 8.0f;  // tau, log2 units: skip the O/l rescale unless the row max grows by more
-  int poly_exp = -1;               // exp2 split: -1 = default, else columns of every 32 on the FMA polynomial
+  int poly_exp = -1;               // exp2 split: columns of every 32 on the FMA polynomial (0,4,8,12,16; -1 = default)
   int bwd_2cta = 1;                // reserved switch for the paired-CTA backward
 };
 Options& options();
@@ -47,9 +47,11 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream);
 
-// Launch the forward kernel for head dim d (64 or 128).  Returns a cudaError_t.
+// Launch the forward kernel for head dim d (64 or 128) with poly_cols of every 32
+// exponentials on the FMA polynomial (0, 4, 8, 12 or 16).  Returns a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, cudaStream_t stream);
+                       const FwdParams& p, int poly_cols, cudaStream_t stream);
+constexpr int kDefaultPolyCols = 0;
 
 // Build a 3-D bf16 tensor map over a contiguous [outer][rows][d] array with a
 // box of 64 x 128 x 1 elements and 128-byte swizzle.  Returns 0 on success.

@@ -253,6 +253,29 @@ FA_DEV float max3f(float a, float b, float c) {
 // The two bf16 values of a packed pair, widened exactly to fp32 (as a packed pair).
 FA_DEV uint64_t bf16x2_widen(uint32_t pk) { return f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)); }
 
+// 2^x for a pair, on the FMA pipe: x = j + f with j = round(x), f in [-1/2, 1/2];
+// 2^f ~ 1 + f (c1 + f (c2 + f c3)) (coefficients from exact_attention_49_gb300/fit_exp2.py,
+// max relative error 1.02e-4); 2^j is added into the exponent field.  x is clamped at
+// -127 so that a masked (-inf) entry gives exactly 0 and no exponent wraps.
+constexpr float kExp2C1 = 6.932829265e-01f;
+constexpr float kExp2C2 = 2.422109611e-01f;
+constexpr float kExp2C3 = 5.500893487e-02f;
+FA_DEV uint64_t ex2_poly2(uint64_t x2) {
+  const float2 xin = f2_unpack(x2);
+  const uint64_t x = f2_pack(fmaxf(xin.x, -127.f), fmaxf(xin.y, -127.f));
+  const uint64_t magic = f2_pack(12582912.f, 12582912.f);  // 1.5 * 2^23: adding it rounds to an integer
+  const uint64_t t = f2_add(x, magic);
+  const uint64_t jf = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const float2 j2 = f2_unpack(jf);
+  const uint64_t f = f2_add(x, f2_pack(-j2.x, -j2.y));
+  uint64_t q = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  q = f2_fma(q, f, f2_pack(kExp2C1, kExp2C1));
+  q = f2_fma(q, f, f2_pack(1.f, 1.f));
+  const float2 qq = f2_unpack(q), tt = f2_unpack(t);
+  return f2_pack(__uint_as_float(__float_as_uint(qq.x) + (__float_as_uint(tt.x) << 23)),
+                 __uint_as_float(__float_as_uint(qq.y) + (__float_as_uint(tt.y) << 23)));
+}
+
 FA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   // cvt.rn.bf16x2.f32 d, a, b puts a in the upper half and b in the lower half.
   uint32_t r;

@@ -137,8 +137,9 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                        ai-papers.net summary, 提案手法 item 2).  0 rescales
  *                        whenever the max grows.
  *   "poly_exp"           exp2 split between the MUFU unit and an FMA-pipe
- *                        polynomial (wiki FA4 (2)): number of columns out of
- *                        every 32 computed by the polynomial, 0..32; -1 = default.
+ *                        polynomial (wiki FA4 (2)) in the forward: number of
+ *                        columns out of every 32 computed by the polynomial,
+ *                        one of 0, 4, 8, 12, 16; -1 = the built-in default.
  * Returns FA_OK or FA_ERR_INVALID_ARG (unknown key or value out of range). */
 int fa_set_option(const char* key, double value);
 int fa_get_option(const char* key, double* value);

@@ -54,6 +54,10 @@ def test_options_roundtrip(L):
     assert fa.fa_set_option("rescale_threshold", -1.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_option("poly_exp", 33) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_option("poly_exp", 2.5) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("poly_exp", 6) == fa.FA_ERR_INVALID_ARG
+    for ok in (-1, 0, 4, 8, 12, 16):
+        assert fa.fa_set_option("poly_exp", ok) == fa.FA_OK
+    assert fa.fa_set_option("poly_exp", -1) == fa.FA_OK
     assert fa.fa_set_option("no_such_option", 1.0) == fa.FA_ERR_INVALID_ARG
 
 

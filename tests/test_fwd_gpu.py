@@ -131,3 +131,16 @@ def test_fwd_long_context_sampled_rows(N, d):
     eo = o_error(to64(o[:, heads][:, :, rows]), o_ref)
     el = max_abs(to64(lse[:, heads][:, :, rows]), lse_ref)
     assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("poly", [0, 4, 8, 12, 16])
+def test_fwd_exp2_split(poly):
+    """Every MUFU / FMA-polynomial exp2 split gives the same answer within tolerance."""
+    old = fa.fa_get_option("poly_exp")
+    try:
+        assert fa.fa_set_option("poly_exp", poly) == fa.FA_OK
+        check_full(1, 4, 4, 2048, 128, True, seed=41)
+        check_full(1, 4, 4, 1024, 128, True, seed=42, qk_mult=4.0)
+        check_full(2, 4, 2, 640, 64, False, seed=43)
+    finally:
+        fa.fa_set_option("poly_exp", old)
