@@ -132,6 +132,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_tflops(flop_per_replica_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every replica's work over the slowest rank's time."""
+    return flop_per_replica_step * world * steps / (max_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -210,8 +225,8 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
-    return {"workload": w.name + ", forward + backward", "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
+def config_of(w, fwd_only=False):
+    return {"workload": w.name + (", forward only" if fwd_only else ", forward + backward"), "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
             "d": w.d, "causal": w.causal, "softmax_scale": "1/sqrt(d)", "seed": w.seed,
             "inputs": "Q,K,V,dO i.i.d. N(0,1) rounded to bf16",
             "l2": "inputs larger than L2: each of Q,K,V,O,dO,dQ,dK,dV is %d MiB (L2 is 129 MB)"
@@ -239,6 +254,9 @@ def run_ours(args, w):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     det = int(args.deterministic)
+    fwd_only = args.fwd_only or not w.backward
+    if args.poly_exp is not None and fa.fa_set_option("poly_exp", args.poly_exp) != fa.FA_OK:
+        raise SystemExit("bad --poly-exp %r" % args.poly_exp)
     ws_bytes = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, det)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -255,6 +273,11 @@ def run_ours(args, w):
         check("fa_fwd", fa.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream))
         if e is not None:
             e[1].record(stream)
+        if fwd_only:
+            if e is not None:
+                e[2].record(stream)
+                e[3].record(stream)
+            return
         check("fa_bwd_preprocess", fa.fa_bwd_preprocess(o, do, lse, B, H, Hkv, N, d, det, wsp, ws_bytes, stream))
         if e is not None:
             e[2].record(stream)
@@ -290,44 +313,44 @@ def run_ours(args, w):
     total_ms = start.elapsed_time(stop)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     main_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / args.steps
     f_fwd = flops_fwd(B, H, N, d, w.causal)
-    f_bwd = 2.5 * f_fwd
-    value = (f_fwd + f_bwd) * ws * args.steps / (total_ms * 1e-3) / 1e12
+    f_bwd = 0.0 if fwd_only else 2.5 * f_fwd
+    value = throughput_tflops(f_fwd + f_bwd, ws, args.steps, total_ms)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    hq, hk, hv, hdo = (x.pin_memory() for x in (q_h, k_h, v_h, do_h))
+    ins = (q_h, k_h, v_h) if fwd_only else (q_h, k_h, v_h, do_h)
+    hq, hk, hv = (x.pin_memory() for x in (q_h, k_h, v_h))
+    hdo = do_h.pin_memory() if not fwd_only else None
     ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q_h, q_h, k_h, v_h))
     hlse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+    outs = (ho, hlse) if fwd_only else (ho, hlse, hdq, hdk, hdv)
+    h2d = sum(x.numel() * x.element_size() for x in ins)
+    d2h = sum(x.numel() * x.element_size() for x in outs)
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
-            dst.copy_(src, non_blocking=True)
+        for dst, src in zip((q, k, v, do), (hq, hk, hv, hdo)):
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
         step()
-        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+        for dst, src in zip(outs, (o, lse, dq, dk, dv)):
             dst.copy_(src, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    e2e_value = None
+    if not args.no_e2e:
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = (f_fwd + f_bwd) * ws * e2e_steps / (float(e2e_ms.item()) * 1e-3) / 1e12
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_value = throughput_tflops(f_fwd + f_bwd, ws, e2e_steps, max_over_ranks(e0.elapsed_time(e1), dev))
 
     if rank != 0:
         if ws > 1:
@@ -338,7 +361,7 @@ def run_ours(args, w):
     timed_s = total_ms * 1e-3
     peak_key = "bf16_tflops_sustained" if timed_s > 1.0 else "bf16_tflops"
     peak = float(peaks[peak_key])
-    dominant = "bwd_main" if main_ms >= fwd_ms else "fwd"
+    dominant = "bwd_main" if (main_ms >= fwd_ms and not fwd_only) else "fwd"
     dom_ms = main_ms if dominant == "bwd_main" else fwd_ms
     dom_flops = f_bwd if dominant == "bwd_main" else f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
@@ -347,26 +370,29 @@ def run_ours(args, w):
                 "peak_source": "%s %s (%s)" % (peak_src, peak_key, "MEASURED_PEAKS.json" if peak_src == "measured"
                                                else "profiling recipe fallback")}
 
-    # ---- CPU baseline: the oracle on this host's cores, bounded sample
-    cpu_val, cpu_s, cpu_heads, cores = cpu_oracle_sample(w, q_h, k_h, v_h, do_h, budget_s=args.cpu_budget)
+    # ---- CPU baseline: the oracle on this host's cores, bounded sample (skipped when the budget is 0)
+    cpu = None
+    if args.cpu_budget > 0:
+        cpu_val, cpu_s, cpu_heads, cores = cpu_oracle_sample(w, q_h, k_h, v_h, do_h, budget_s=args.cpu_budget)
+        cpu = {"value": cpu_val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": "%d whole heads (forward + backward, fp64) of the workload, %.1f s" % (cpu_heads, cpu_s)}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, fwd_only),
         "pct_of_peak": {"measured_bf16": value / ws / peak, "nominal_2250": value / ws / NOMINAL_PEAK_TFLOPS},
         "fwd": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
                 "frac_of_nominal_2250": f_fwd / (fwd_ms * 1e-3) / 1e12 / NOMINAL_PEAK_TFLOPS},
-        "bwd": {"ms": ms_step - fwd_ms, "tflops": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12,
-                "main_ms": main_ms,
-                "frac_of_nominal_2250": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12 / NOMINAL_PEAK_TFLOPS},
+        "bwd": None if fwd_only else {
+            "ms": ms_step - fwd_ms, "tflops": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12, "main_ms": main_ms,
+            "frac_of_nominal_2250": f_bwd / ((ms_step - fwd_ms) * 1e-3) / 1e12 / NOMINAL_PEAK_TFLOPS},
         "deterministic": bool(det),
         "roofline": roofline,
-        "cpu_baseline": {"value": cpu_val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d whole heads (forward + backward, fp64) of the workload, %.1f s"
-                                   % (cpu_heads, cpu_s)},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "cpu_baseline": cpu,
+        "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                                               "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": (1 if fwd_only else 4) * args.steps,
+        "poly_exp": fa.fa_get_option("poly_exp"),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -385,11 +411,16 @@ def main():
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling on a smaller case)")
+    ap.add_argument("--seq", type=int, default=65536, help="N for the long-context workload C5")
+    ap.add_argument("--head-dim", type=int, default=128, help="d for the long-context workload C5")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward alone")
+    ap.add_argument("--poly-exp", type=int, default=None, help="exp2 split: columns of 32 on the FMA polynomial")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    from exact_attention_49_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from exact_attention_49_gb300.inputs import WORKLOADS, long_context
+    w = long_context(args.seq, args.head_dim) if args.workload == "C5" else WORKLOADS[args.workload]
     if args.batch:
         import dataclasses
         w = dataclasses.replace(w, B=args.batch, name=w.name.replace("B%d " % w.B, "B%d " % args.batch))

@@ -150,9 +150,9 @@ int fa_set_option(const char* key, double value) {
     options().poly_exp = static_cast<int>(value);
     return FA_OK;
   }
-  if (!std::strcmp(key, "bwd_2cta")) {
+  if (!std::strcmp(key, "debug_drop_kv_load")) {
     if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
-    options().bwd_2cta = static_cast<int>(value);
+    options().debug_drop_kv_load = static_cast<int>(value);
     return FA_OK;
   }
   return FA_ERR_INVALID_ARG;
@@ -162,7 +162,7 @@ int fa_get_option(const char* key, double* value) {
   if (!key || !value) return FA_ERR_INVALID_ARG;
   if (!std::strcmp(key, "rescale_threshold")) { *value = options().rescale_threshold; return FA_OK; }
   if (!std::strcmp(key, "poly_exp")) { *value = options().poly_exp; return FA_OK; }
-  if (!std::strcmp(key, "bwd_2cta")) { *value = options().bwd_2cta; return FA_OK; }
+  if (!std::strcmp(key, "debug_drop_kv_load")) { *value = options().debug_drop_kv_load; return FA_OK; }
   return FA_ERR_INVALID_ARG;
 }
 
@@ -205,6 +205,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.tau = options().rescale_threshold;
+  p.drop_it = options().debug_drop_kv_load ? 2 : -1;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(320, 1)
       int issued = 0;
       for (int it = 0; it < 2 * n_kv; ++it) {
         const int slot = it % C::STAGES;
+        if (it == p.drop_it) continue;  // failure-injection test hook (never set in normal use)
         if (!mbar_wait(empty_bar(slot), ((it / C::STAGES) & 1) ^ 1, abort, p.status)) break;
         mbar_arrive_expect_tx(full_bar(slot), C::TILE);
         for (int ch = 0; ch < C::CHUNKS; ++ch)

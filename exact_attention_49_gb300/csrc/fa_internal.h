@@ -12,7 +12,7 @@ namespace fa {
 struct Options {
   float rescale_threshold = 8.0f;  // tau, log2 units: skip the O/l rescale unless the row max grows by more
   int poly_exp = -1;               // exp2 split: columns of every 32 on the FMA polynomial (0,4,8,12,16; -1 = default)
-  int bwd_2cta = 1;                // reserved switch for the paired-CTA backward
+  int debug_drop_kv_load = 0;      // failure-injection test hook: the forward skips one K/V load
 };
 Options& options();
 
@@ -24,6 +24,7 @@ struct FwdParams {
   float scale_log2;  // softmax scale * log2(e)
   float tau;         // rescale threshold, log2 units
   int* status;       // device status word
+  int drop_it;       // failure-injection test hook: K/V load index the producer skips (-1: none)
 };
 
 struct BwdParams {

@@ -140,6 +140,12 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                        polynomial (wiki FA4 (2)) in the forward: number of
  *                        columns out of every 32 computed by the polynomial,
  *                        one of 0, 4, 8, 12, 16; -1 = the built-in default.
+ *   "debug_drop_kv_load" failure-injection test hook, 0 (default) or 1: the
+ *                        forward's copy warp skips its second K/V tile load, so
+ *                        the MMA warp's bounded wait gives up (after ~2 s), the
+ *                        CTA drains and exits, and fa_last_device_status()
+ *                        returns FA_ERR_DEVICE_TIMEOUT.  Output is undefined
+ *                        while it is set.
  * Returns FA_OK or FA_ERR_INVALID_ARG (unknown key or value out of range). */
 int fa_set_option(const char* key, double value);
 int fa_get_option(const char* key, double* value);

@@ -11,6 +11,9 @@ Tolerances (stated for the hot path):
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 O_TOL = 1e-2
@@ -52,3 +55,13 @@ def rel_fro(g, g_ref) -> float:
 def to64(t) -> np.ndarray:
     """torch tensor (any device, any float dtype) -> numpy float64."""
     return t.detach().to("cpu").double().numpy()
+
+
+def record(test: str, **metrics) -> None:
+    """Append the measured errors of one parity check to $FA_PARITY_LOG (JSON lines)."""
+    path = os.environ.get("FA_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": test, **{k: (float(v) if isinstance(v, (float, np.floating)) else v)
+                                             for k, v in metrics.items()}}) + "\n")

@@ -59,6 +59,8 @@ def test_options_roundtrip(L):
         assert fa.fa_set_option("poly_exp", ok) == fa.FA_OK
     assert fa.fa_set_option("poly_exp", -1) == fa.FA_OK
     assert fa.fa_set_option("no_such_option", 1.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("debug_drop_kv_load", 2) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_get_option("debug_drop_kv_load") == 0.0
 
 
 P = ctypes.c_void_p

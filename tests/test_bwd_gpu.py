@@ -14,7 +14,7 @@ import torch
 from exact_attention_49_gb300 import binding as fa
 from exact_attention_49_gb300.inputs import WORKLOADS, make_inputs
 from oracle import reference as ref
-from parity import GRAD_RTOL, rel_fro, to64
+from parity import GRAD_RTOL, record, rel_fro, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,8 @@ def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0, deterministic=False):
     dq, dk, dv = gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic)
     rq, rk, rv = ref.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, scale)
     errs = (rel_fro(to64(dq), rq), rel_fro(to64(dk), rk), rel_fro(to64(dv), rv))
+    record("bwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=qk_mult, deterministic=bool(deterministic),
+           dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2])
     assert max(errs) <= GRAD_RTOL, errs
     return errs
 
@@ -127,4 +129,6 @@ def test_bwd_full_size_sampled(name, det):
                                   to64(do[b:b + 1, hs]), w.causal, w.scale)
         errs = (rel_fro(to64(dq[b:b + 1, hs]), rq), rel_fro(to64(dk[b:b + 1, g:g + 1]), rk),
                 rel_fro(to64(dv[b:b + 1, g:g + 1]), rv))
+        record("bwd_full_size", workload=w.name, deterministic=bool(det), group=[b, g], dq_rel=errs[0],
+               dk_rel=errs[1], dv_rel=errs[2])
         assert max(errs) <= GRAD_RTOL, ((b, g), errs)

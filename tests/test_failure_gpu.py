@@ -1,0 +1,48 @@
+"""The device-side failure path, exercised without faulting the GPU.
+
+Every wait inside the kernels is bounded.  The "debug_drop_kv_load" test hook
+makes the forward's copy warp skip one K/V tile load, so the MMA warp's wait
+for it runs out (about 2 s): the CTA raises its abort flag, the other roles stop
+waiting, in-flight copies and MMAs drain, tensor memory is freed and the kernel
+returns normally; fa_last_device_status() then reports FA_ERR_DEVICE_TIMEOUT.
+The next call on the same context must work and be correct.
+"""
+import pytest
+import torch
+
+from exact_attention_49_gb300 import binding as fa
+from exact_attention_49_gb300.inputs import make_inputs
+from oracle import reference as ref
+from parity import LSE_TOL, O_TOL, max_abs, o_error, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_attention_49_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.lib()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    B, H, Hkv, N, d = 1, 1, 1, 512, 64
+    q, k, v, _ = make_inputs(B, H, Hkv, N, d, seed=5)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert fa.fa_set_option("debug_drop_kv_load", 1) == fa.FA_OK
+    try:
+        fa.attention_forward(qd, kd, vd, causal=False)
+        torch.cuda.synchronize()
+        assert fa.fa_last_device_status() == fa.FA_ERR_DEVICE_TIMEOUT
+    finally:
+        assert fa.fa_set_option("debug_drop_kv_load", 0) == fa.FA_OK
+    # the status was cleared by the read; the context is healthy and results are right
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = fa.attention_forward(qd, kd, vd, causal=False)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o_ref, lse_ref = ref.attn_fwd(to64(q), to64(k), to64(v), False, d ** -0.5)
+    assert o_error(to64(o), o_ref) <= O_TOL
+    assert max_abs(to64(lse), lse_ref) <= LSE_TOL

@@ -14,7 +14,7 @@ import torch
 from exact_attention_49_gb300 import binding as fa
 from exact_attention_49_gb300.inputs import WORKLOADS, long_context, make_inputs
 from oracle import reference as ref
-from parity import LSE_TOL, O_TOL, max_abs, o_error, to64
+from parity import LSE_TOL, O_TOL, max_abs, o_error, record, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,9 @@ def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0):
     o, lse = run_fwd(q, k, v, causal, scale)
     o_ref, lse_ref = ref.attn_fwd(to64(q), to64(k), to64(v), causal, scale)
     eo, el = o_error(to64(o), o_ref), max_abs(to64(lse), lse_ref)
+    record("fwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=qk_mult, o_err=eo, lse_err=el,
+           o_maxabs=max_abs(to64(o), o_ref), poly=fa.fa_get_option("poly_exp"),
+           tau=fa.fa_get_option("rescale_threshold"))
     assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
     return eo, el
 
@@ -109,6 +112,8 @@ def check_big_heads(w):
                                       to64(v[b:b + 1, g:g + 1]), w.causal, w.scale)
         eo = o_error(to64(o[b:b + 1, h:h + 1]), o_ref)
         el = max_abs(to64(lse[b:b + 1, h:h + 1]), lse_ref)
+        record("fwd_full_size", workload=w.name, head=[b, h], o_err=eo, lse_err=el,
+               o_maxabs=max_abs(to64(o[b:b + 1, h:h + 1]), o_ref))
         assert eo <= O_TOL and el <= LSE_TOL, ((b, h), eo, el)
 
 
@@ -130,6 +135,7 @@ def test_fwd_long_context_sampled_rows(N, d):
     o_ref, lse_ref = ref.attn_fwd(to64(qs), to64(k[:, heads]), to64(v[:, heads]), True, w.scale, qpos=rows)
     eo = o_error(to64(o[:, heads][:, :, rows]), o_ref)
     el = max_abs(to64(lse[:, heads][:, :, rows]), lse_ref)
+    record("fwd_long_context", workload=w.name, rows=int(len(rows)), heads=heads, o_err=eo, lse_err=el)
     assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
 
 
