@@ -15,9 +15,8 @@
 //                  S^T  = K_j Q_i^T        (TMEM, fp32)
 //                  dP^T = V_j dO_i^T       (TMEM, fp32)
 //                  P^T  = exp2(S^T * scale*log2e - lse2_i)     (bf16, over S^T in TMEM)
-//                  dS^T = P^T * (dP^T - D_i) * scale           (bf16, over dP^T in TMEM
-//                                                               and in shared memory)
-//                  dV  += P^T dO_i,  dK += dS^T Q_i            (A operand from TMEM)
+//                  dS^T = P^T * (dP^T - D_i) * scale           (bf16, in shared memory)
+//                  dV  += P^T dO_i  (A from TMEM),  dK += dS^T Q_i  (A from shared memory)
 //                  dQ_i = dS K_j                               (TMEM, then fp32
 //                                                               reductions into the
 //                                                               dQ accumulator)
@@ -39,7 +38,7 @@
 //   warp 12     MMA issuer (one thread) and TMEM allocator
 //   warp 13     TMA producer (one thread)
 //   warps 14-15 idle
-// Tensor memory (512 columns): dV | dK | S^T (later P^T) | dP^T (later dS^T, then dQ_i).
+// Tensor memory (512 columns): dV | dK | S^T (later P^T) | dP^T (then dQ_i).
 #include <algorithm>
 
 #include "fa_internal.h"
@@ -245,7 +244,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (!(ok = mbar_wait(ds_ready, t & 1, abort, p.status))) break;
         tc_fence_after();
-        ts_acc(C::COL_DK, C::COL_DP, sQ(s), t > 0);  // dK += dS^T Q_t
+        // dQ first, so its read-out overlaps the dK MMA
         if constexpr (C::DQ_T) {
           // dQ_t^T = K_j^T dS^T (M = d, N = queries) into the dP^T columns: TMEM lane = head-dim
           // column, so the read-out warps reduce 128 contiguous bytes per instruction
@@ -260,6 +259,12 @@ __global__ void __launch_bounds__(512, 1)
                    sdesc_sw128(sK + kk * 2048, 16384, 1024), idQ, kk > 0);
         }
         mma_commit(dq_full);
+        // dK += dS^T Q_t, with dS^T read from shared memory as a K-major operand (rows = keys,
+        // 64 queries per 128-byte swizzled row chunk): the same bytes the dQ MMA reads
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(sQ(s) + kk * 2048, 16384, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(st_empty(s));
         if (more) {
           if (!(ok = mbar_wait(dq_empty, t & 1, abort, p.status))) break;
@@ -352,7 +357,6 @@ __global__ void __launch_bounds__(512, 1)
             pk[2 * c4] = pack_bf16x2(d01.x, d01.y);
             pk[2 * c4 + 1] = pack_bf16x2(d23.x, d23.y);
           }
-          tmem_st16(tDP + 16 * cc, pk);
           // dS^T row r, queries [32cc, 32cc+32) of this half: four 16-byte pieces, 128B-swizzled
 #pragma unroll
           for (int pc = 0; pc < 4; ++pc) {
@@ -362,9 +366,8 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
+      fence_async_smem();  // dS^T visible to the MMAs (async proxy)
+      tc_fence_before();   // our TMEM loads of dP^T are done before the dQ MMA overwrites it
       mbar_arrive(ds_ready);
     }
   } else if (warp < 12) {
