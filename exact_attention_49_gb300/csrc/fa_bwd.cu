@@ -200,82 +200,83 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
-      constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);
-      constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);
-      auto ss_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t bsm) {
+    // The whole warp runs this loop converged; lane 0 issues the MMAs and commits.
+    const uint32_t leader = (lane == 0) ? 1u : 0u;
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);
+    constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);
+    auto ss_kmajor = [&](uint32_t dcol, uint32_t a, uint32_t bsm) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bsm + off, 16, 1024), idS, kk > 0);
-        }
-      };
-      // D[128 keys x D] += A^T(TMEM, P^T or dS^T) * B(smem, M... [queries][D], MN-major)
-      auto ts_acc = [&](uint32_t dcol, uint32_t acol, uint32_t bsm, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + dcol, tmem + acol + 64 * (kk >> 2) + (kk & 3) * 8, sdesc_sw128(bsm + kk * 2048, 16384, 1024),
-                 idKV, (acc || kk > 0) ? 1u : 0u);
-      };
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
-      auto sQ = [&](int s) { return sbase + C::OFF_Q + s * C::TILE; };
-      auto sDO = [&](int s) { return sbase + C::OFF_DO + s * C::TILE; };
-      bool ok = mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(st_full(0), 0, abort, p.status);
-      if (ok) {
-        tc_fence_after();
-        ss_kmajor(C::COL_S, sK, sQ(0));
-        mma_commit(s_full);
-        ss_kmajor(C::COL_DP, sV, sDO(0));
-        mma_commit(dp_full);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bsm + off, 16, 1024), idS, kk > 0, leader);
       }
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t & 1;
-        const bool more = t + 1 < ntiles;
-        if (!(ok = mbar_wait(p_ready, t & 1, abort, p.status))) break;
-        tc_fence_after();
-        ts_acc(C::COL_DV, C::COL_S, sDO(s), t > 0);  // dV += P^T dO_t
-        if (more) {
-          if (!(ok = mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status))) break;
-          tc_fence_after();
-          ss_kmajor(C::COL_S, sK, sQ(s ^ 1));  // S^T of the next tile (P^T_t already consumed)
-          mma_commit(s_full);
-        }
-        if (!(ok = mbar_wait(ds_ready, t & 1, abort, p.status))) break;
-        tc_fence_after();
-        // dQ first, so its read-out overlaps the dK MMA
-        if constexpr (C::DQ_T) {
-          // dQ_t^T = K_j^T dS^T (M = d, N = queries) into the dP^T columns: TMEM lane = head-dim
-          // column, so the read-out warps reduce 128 contiguous bytes per instruction
+    };
+    // D[128 keys x D] += A^T(TMEM, P^T or dS^T) * B(smem, M... [queries][D], MN-major)
+    auto ts_acc = [&](uint32_t dcol, uint32_t acol, uint32_t bsm, bool acc) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::COL_DP, sdesc_sw128(sK + kk * 2048, 16384, 1024),
-                   sdesc_sw128(sDS + kk * 2048, 16384, 1024), idQT, kk > 0);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K_j, into the dP^T columns
-            mma_ss(tmem + C::COL_DP, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
-                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idQ, kk > 0);
-        }
-        mma_commit(dq_full);
-        // dK += dS^T Q_t, with dS^T read from shared memory as a K-major operand (rows = keys,
-        // 64 queries per 128-byte swizzled row chunk): the same bytes the dQ MMA reads
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(sQ(s) + kk * 2048, 16384, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(st_empty(s));
-        if (more) {
-          if (!(ok = mbar_wait(dq_empty, t & 1, abort, p.status))) break;
-          tc_fence_after();
-          ss_kmajor(C::COL_DP, sV, sDO(s ^ 1));
-          mma_commit(dp_full);
-        }
-      }
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, abort, p.status);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + dcol, tmem + acol + 64 * (kk >> 2) + (kk & 3) * 8, sdesc_sw128(bsm + kk * 2048, 16384, 1024),
+               idKV, (acc || kk > 0) ? 1u : 0u, leader);
+    };
+    const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+    auto sQ = [&](int s) { return sbase + C::OFF_Q + s * C::TILE; };
+    auto sDO = [&](int s) { return sbase + C::OFF_DO + s * C::TILE; };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, p.status));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(st_full(0), 0, abort, p.status));
+    if (ok) {
+      tc_fence_after();
+      ss_kmajor(C::COL_S, sK, sQ(0));
+      mma_commit(s_full, leader);
+      ss_kmajor(C::COL_DP, sV, sDO(0));
+      mma_commit(dp_full, leader);
     }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int s = t & 1;
+      const bool more = t + 1 < ntiles;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, abort, p.status)))) break;
+      tc_fence_after();
+      ts_acc(C::COL_DV, C::COL_S, sDO(s), t > 0);  // dV += P^T dO_t
+      if (more) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status)))) break;
+        tc_fence_after();
+        ss_kmajor(C::COL_S, sK, sQ(s ^ 1));  // S^T of the next tile (P^T_t already consumed)
+        mma_commit(s_full, leader);
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_ready, t & 1, abort, p.status)))) break;
+      tc_fence_after();
+      // dQ first, so its read-out overlaps the dK MMA
+      if constexpr (C::DQ_T) {
+        // dQ_t^T = K_j^T dS^T (M = d, N = queries) into the dP^T columns: TMEM lane = head-dim
+        // column, so the read-out warps reduce 128 contiguous bytes per instruction
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::COL_DP, sdesc_sw128(sK + kk * 2048, 16384, 1024),
+                 sdesc_sw128(sDS + kk * 2048, 16384, 1024), idQT, kk > 0, leader);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ_t = dS K_j, into the dP^T columns
+          mma_ss(tmem + C::COL_DP, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
+                 sdesc_sw128(sK + kk * 2048, 16384, 1024), idQ, kk > 0, leader);
+      }
+      mma_commit(dq_full, leader);
+      // dK += dS^T Q_t, with dS^T read from shared memory as a K-major operand (rows = keys,
+      // 64 queries per 128-byte swizzled row chunk): the same bytes the dQ MMA reads
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+               sdesc_sw128(sQ(s) + kk * 2048, 16384, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u, leader);
+      mma_commit(st_empty(s), leader);
+      if (more) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_empty, t & 1, abort, p.status)))) break;
+        tc_fence_after();
+        ss_kmajor(C::COL_DP, sV, sDO(s ^ 1));
+        mma_commit(dp_full, leader);
+      }
+    }
+    mma_commit(mma_done, leader);
+    __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
   } else if (warp < 8) {
     // ------------------------------------------------------------ compute: P^T and dS^T
     const int w = warp >> 2;           // query-column half
@@ -459,9 +460,9 @@ __global__ void __launch_bounds__(512, 1)
         if (r == 0) st_release(counter, j + 1);
       }
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (ntiles - 1) & 1, abort, p.status));
+    // mma_done is committed after every MMA of the CTA, the last dK one included
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
     if (ok) {
-      // every MMA has completed (dq_full of the last tile is committed after all of them)
       tc_fence_after();
       const size_t krow = (size_t)bg * N + (size_t)j * 128 + r;
 #pragma unroll
