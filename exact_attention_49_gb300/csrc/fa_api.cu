@@ -213,18 +213,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 
-// Workspace layout: [dQ accumulator fp32 rows*d][lse2 fp32 rows][D fp32 rows][counters int32 B*H*N/128]
+// Workspace layout, with the rows of every head padded to Np = N rounded up to 128:
+// [dQ accumulator fp32 B*H*Np*d][lse2 fp32 B*H*Np][D fp32 B*H*Np][counters int32 B*H*Np/128]
 struct BwdWorkspace {
   size_t off_lse2, off_d, off_cnt, total;
 };
 static BwdWorkspace bwd_ws_layout(int B, int H, int N, int d, int deterministic) {
-  const size_t rows = (size_t)B * H * N;
+  const size_t Np = ((size_t)N + 127) / 128 * 128;
+  const size_t rows = (size_t)B * H * Np;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdWorkspace w;
   w.off_lse2 = up(rows * d * 4);
   w.off_d = up(w.off_lse2 + rows * 4);
   w.off_cnt = up(w.off_d + rows * 4);
-  w.total = w.off_cnt + (deterministic ? up((size_t)B * H * ((N + 127) / 128) * 4) : 0);
+  w.total = w.off_cnt + (deterministic ? up(rows / 128 * 4) : 0);
   return w;
 }
 
@@ -241,7 +243,6 @@ static int check_bwd_common(int B, int H, int Hkv, int N, int d, int determinist
   int st = check_shape(B, H, Hkv, N, d);
   if (st) return st;
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
-  if (N % 128 != 0) return fail_detail(FA_ERR_UNSUPPORTED, "backward needs N % 128 == 0");
   if (B == 0 || N == 0) return 1;
   if (!ws) return FA_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return FA_ERR_MISALIGNED;
@@ -259,11 +260,11 @@ int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, 
   if ((st = check_device())) return st;
   const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const long long rows = (long long)B * H * N;
+  const long long heads = (long long)B * H;
   cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float*>(ws + w.off_lse2),
                                  reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws),
-                                 deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr,
-                                 rows, (long long)B * H * (N / 128), static_cast<cudaStream_t>(stream));
+                                 deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr, heads, N,
+                                 heads * ((N + 127) / 128), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
 }
 
@@ -317,7 +318,7 @@ int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, int determ
   if (!dq) return FA_ERR_INVALID_ARG;
   if (!aligned(dq, 16)) return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
-  cudaError_t e = launch_bwd_post(static_cast<const float*>(workspace), dq, (long long)B * H * N * d,
+  cudaError_t e = launch_bwd_post(static_cast<const float*>(workspace), dq, (long long)B * H, N, d,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_postprocess launch", e);
 }

@@ -112,14 +112,17 @@ __global__ void __launch_bounds__(512, 1)
 
   // ---- work unit
   const int N = p.N;
-  const int nq = N / 128;
+  // Rows are padded per head to Np, a multiple of 128, in the workspace arrays (lse2, D,
+  // dQ accumulator); the last tiles of Q, dO, K, V read zeros past N (TMA out-of-bounds fill).
+  const int Np = (N + 127) & ~127;
+  const int nq = Np / 128;
   const int BG = p.B * p.Hkv;
   // CTA order: groups of (up to) 8 K/V heads, key tiles heaviest first (j = 0) within a
   // group.  The CTAs resident at any time then share few heads' Q/dO tiles and dQ
   // accumulator lines, which stay in L2 (about 14% faster than key-tile-major order
   // over all heads on the B4 H16 N8192 workload).
   constexpr int kHeadGroup = 8;
-  const int nkv = N / 128;
+  const int nkv = Np / 128;
   const int gi = blockIdx.x / (kHeadGroup * nkv);
   const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
   const int rem = blockIdx.x - gi * kHeadGroup * nkv;
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_3d(sbase + C::OFF_Q + s * C::TILE + ch * 16384, &tm_q, st_full(s), ch * 64, i * 128, bh);
           tma_load_3d(sbase + C::OFF_DO + s * C::TILE + ch * 16384, &tm_do, st_full(s), ch * 64, i * 128, bh);
         }
-        const size_t row0 = (size_t)bh * N + (size_t)i * 128;
+        const size_t row0 = (size_t)bh * Np + (size_t)i * 128;
         bulk_load(sbase + C::OFF_LD + s * 1024, p.lse2 + row0, 512, st_full(s));
         bulk_load(sbase + C::OFF_LD + s * 1024 + 512, p.dvec + row0, 512, st_full(s));
         issued = t + 1;
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t scx2 = f2_pack(p.scale, p.scale);
     uint8_t* ds_row = smem + C::OFF_DS + w * 16384 + r * 128;
+    const bool key_pad = j * 128 + r >= N;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
       const bool diag = p.causal && tile_row(t) == j;
@@ -299,11 +303,11 @@ __global__ void __launch_bounds__(512, 1)
       {
         uint32_t ra[32], rb[32];
         tmem_ld32_nowait(tS, ra);
-        tmem_ld32_nowait(tS + 32, rb);
         tmem_wait_ld(ra);
-        tmem_wait_ld(rb);
+        tmem_ld32_nowait(tS + 32, rb);  // in flight while the first 32 columns are processed
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
+          if (c4 == 8) tmem_wait_ld(rb);
           const float4 L = lse4[c4];
           const uint32_t* src = (c4 < 8) ? ra : rb;
           const int o = (c4 & 7) * 4;
@@ -316,6 +320,10 @@ __global__ void __launch_bounds__(512, 1)
           pv[4 * c4 + 2] = ex2_mufu(x23.x);
           pv[4 * c4 + 3] = ex2_mufu(x23.y);
         }
+      }
+      if (key_pad) {  // a key row past N (zero-filled K) carries no probability
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = 0.f;
       }
       if (diag) {  // key r > query q is masked on the diagonal tile
 #pragma unroll
@@ -338,11 +346,11 @@ __global__ void __launch_bounds__(512, 1)
       {
         uint32_t ra[32], rb[32];
         tmem_ld32_nowait(tDP, ra);
-        tmem_ld32_nowait(tDP + 32, rb);
         tmem_wait_ld(ra);
-        tmem_wait_ld(rb);
+        tmem_ld32_nowait(tDP + 32, rb);  // in flight while the first 32 columns are processed
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
+          if (cc == 1) tmem_wait_ld(rb);
           const uint32_t* src = cc ? rb : ra;
           uint32_t pk[16];
 #pragma unroll
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(512, 1)
       if constexpr (C::DQ_T) {
         // thread r holds column r of dQ_i (rows q = 0..127).  Read rows 0-63, reduce
         // them, read rows 64-127, hand the TMEM columns back to the MMA warp, reduce.
-        float* col = p.dq_acc + ((size_t)bh * N + (size_t)i * 128) * D + r;
+        float* col = p.dq_acc + ((size_t)bh * Np + (size_t)i * 128) * D + r;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t va[32], vb[32];
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       } else {
-        float* dst = p.dq_acc + ((size_t)bh * N + (size_t)i * 128 + r) * D;
+        float* dst = p.dq_acc + ((size_t)bh * Np + (size_t)i * 128 + r) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
@@ -465,6 +473,7 @@ __global__ void __launch_bounds__(512, 1)
     if (ok) {
       tc_fence_after();
       const size_t krow = (size_t)bg * N + (size_t)j * 128 + r;
+      const bool krow_valid = j * 128 + r < N;  // the last key tile may run past N
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which ? p.dk : p.dv) + krow * D);
@@ -475,7 +484,8 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(tcol + 32 * c, v);
 #pragma unroll
           for (int m = 0; m < 4; ++m)
-            out[4 * c + m] =
+            if (krow_valid)
+              out[4 * c + m] =
                 make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]), __uint_as_float(v[8 * m + 1])),
                            pack_bf16x2(__uint_as_float(v[8 * m + 2]), __uint_as_float(v[8 * m + 3])),
                            pack_bf16x2(__uint_as_float(v[8 * m + 4]), __uint_as_float(v[8 * m + 5])),
@@ -494,43 +504,63 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ---------------------------------------------------------------- preprocess
-// One warp per query row: D = sum_c dO_c * O_c (fp32 products of bf16 inputs),
-// lse2 = LSE * log2(e).  Then zero the dQ accumulator and the counters.
+// Per (padded) query row: D = sum_c dO_c * O_c (fp32 products of bf16 inputs) and
+// lse2 = LSE * log2(e); rows past N of each head get lse2 = +inf (so P = 0 there) and D = 0.
+// A warp takes four rows at a time, eight lanes per row, 16-byte loads.  Then zero the dQ
+// accumulator (padded rows included) and the counters.
+FA_DEV float dot_bf16x8(uint4 x, uint4 y, float acc) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
+    acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+  }
+  return acc;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ lse2,
                                                       float* __restrict__ dvec,
                                                       float4* __restrict__ dq_acc, int* __restrict__ counters,
-                                                      long long rows, long long n_counters) {
-  constexpr int PER = D / 32;  // bf16 elements per lane
+                                                      long long heads, int N, int Np, long long n_counters) {
+  constexpr int V = D / 64;  // 16-byte vectors per lane (eight lanes per row)
   const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
   const long long gw = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (long long row = gw; row < rows; row += nwarps) {
-    const uint16_t* a = o + row * D + lane * PER;
-    const uint16_t* c = dout + row * D + lane * PER;
+  const int sub = lane & 7;
+  const long long quads = heads * Np / 4;  // Np is a multiple of 128, so a quad stays in one head
+  for (long long qd = gw; qd < quads; qd += nwarps) {
+    const long long prow = 4 * qd + (lane >> 3);
+    long long row = prow;
+    bool valid = true;
+    if (N != Np) {
+      const long long bh = prow / Np;
+      const int n = static_cast<int>(prow - bh * Np);
+      valid = n < N;
+      row = bh * N + n;
+    }
     float acc = 0.f;
-    if (PER == 4) {
-      const uint2 x = *reinterpret_cast<const uint2*>(a), y = *reinterpret_cast<const uint2*>(c);
-      const uint32_t xs[2] = {x.x, x.y}, ys[2] = {y.x, y.y};
+    if (valid) {
+      const uint4* a = reinterpret_cast<const uint4*>(o + row * D) + sub * V;
+      const uint4* c = reinterpret_cast<const uint4*>(dout + row * D) + sub * V;
+      uint4 xa[V], xc[V];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+      for (int k = 0; k < V; ++k) {
+        xa[k] = a[k];
+        xc[k] = c[k];
       }
-    } else {
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(a), y = *reinterpret_cast<const uint32_t*>(c);
-      acc = fmaf(__uint_as_float(x << 16), __uint_as_float(y << 16), acc);
-      acc = fmaf(__uint_as_float(x & 0xffff0000u), __uint_as_float(y & 0xffff0000u), acc);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc = dot_bf16x8(xa[k], xc[k], acc);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      lse2[row] = lse[row] * 1.4426950408889634f;
-      dvec[row] = acc;
+    for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0) {
+      lse2[prow] = valid ? lse[row] * 1.4426950408889634f : INFINITY;
+      dvec[prow] = valid ? acc : 0.f;
     }
   }
-  const long long n4 = rows * D / 4;
+  const long long n4 = heads * Np * D / 4;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthr = (long long)gridDim.x * blockDim.x;
   for (long long k = tid; k < n4; k += nthr) dq_acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -539,11 +569,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 }
 
 // ---------------------------------------------------------------- postprocess
-// dQ (bf16) = accumulator (fp32; the softmax scale is already folded into dS).
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4) {
+// dQ (bf16, [heads][N][d]) = accumulator (fp32, [heads][Np][d]; the softmax scale is already
+// folded into dS).
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4,
+                                                       int d4, int N, int Np) {
   const long long nthr = (long long)gridDim.x * blockDim.x;
   for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += nthr) {
-    const float4 x = acc[k];
+    long long src = k;
+    if (N != Np) {
+      const long long row = k / d4;
+      const long long bh = row / N;
+      src = ((bh * Np + (row - bh * N)) * d4) + (k - row * d4);
+    }
+    const float4 x = acc[src];
     dq[k] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
   }
 }
@@ -561,24 +599,28 @@ static int sm_count() {
 }
 
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
-                           float* dq_acc, int* counters, long long rows, long long n_counters, cudaStream_t stream) {
-  const long long want = (rows + 7) / 8;
+                           float* dq_acc, int* counters, long long heads, int N, long long n_counters,
+                           cudaStream_t stream) {
+  const int Np = (N + 127) & ~127;
+  const long long want = (heads * Np / 4 + 7) / 8;
   const int grid = (int)std::min<long long>(std::max<long long>(want, 1), (long long)sm_count() * 8);
   if (d == 64)
     bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                                 lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, rows,
-                                                 n_counters);
+                                                 lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, heads,
+                                                 N, Np, n_counters);
   else
     bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                                  lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, rows,
-                                                  n_counters);
+                                                  lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, heads,
+                                                  N, Np, n_counters);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream) {
-  const long long n4 = n / 4;
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream) {
+  const int Np = (N + 127) & ~127;
+  const long long n4 = heads * N * d / 4;
   const int grid = (int)std::min<long long>(std::max<long long>((n4 + 255) / 256, 1), (long long)sm_count() * 8);
-  bwd_post_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4);
+  bwd_post_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4,
+                                            d / 4, N, Np);
   return cudaGetLastError();
 }
 
@@ -595,7 +637,7 @@ static cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)(p.N / 128) * p.B * p.Hkv;
+  const long long blocks = (long long)((p.N + 127) / 128) * p.B * p.Hkv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   bwd_main_kernel<D><<<dim3((unsigned)blocks), dim3(512), C::SMEM, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();

@@ -43,10 +43,11 @@ struct BwdParams {
 };
 
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
-                           float* dq_acc, int* counters, long long rows, long long n_counters, cudaStream_t stream);
+                           float* dq_acc, int* counters, long long heads, int N, long long n_counters,
+                           cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long n, cudaStream_t stream);
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
 
 // Launch the forward kernel for head dim d (64 or 128) with poly_cols of every 32
 // exponentials on the FMA polynomial (0, 4, 8, 12 or 16).  Returns a cudaError_t.

@@ -41,8 +41,7 @@
  * device status word, read and cleared by fa_last_device_status.
  *
  * Supported: d in {64, 128}; H % Hkv == 0; 16-byte aligned bf16 pointers,
- * 4-byte aligned lse; N >= 0, any N for the forward, N % 128 == 0 for the
- * backward; scale finite and > 0; an sm_103 device.
+ * 4-byte aligned lse; any N >= 0; scale finite and > 0; an sm_103 device.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -69,8 +68,9 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
 
-/* Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
- * [B,H,N,d], one (LSE in log2 units, D) fp32 pair per query row, and
+/* Bytes of device workspace fa_bwd needs, with the rows of every head padded
+ * to Np = N rounded up to a multiple of 128: the fp32 dQ accumulator
+ * [B,H,Np,d], one (LSE in log2 units, D) fp32 pair per padded query row, and
  * (deterministic mode) one int32 ordering counter per (b, h, 128-row query
  * block).  The workspace must be 256-byte aligned.  0 on bad sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic);

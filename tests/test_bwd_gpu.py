@@ -74,6 +74,32 @@ def test_bwd_gqa_small(causal, d, det):
     check_full(2, 8, 2, 512, d, causal, seed=17, deterministic=det)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 77, 200, 333, 1000])
+def test_bwd_ragged(N, causal, d):
+    """N not a multiple of 128: the last query and key tiles run past N (TMA zero fill, padded
+    workspace rows, masked key rows).  Every head is compared on its own, so a tile that
+    spilled into a neighbouring head's rows would show up."""
+    B, H, Hkv = 2, 4, 2
+    q, k, v, do = make_inputs(B, H, Hkv, N, d, seed=300 + N + d)
+    scale = d ** -0.5
+    dq, dk, dv = gpu_fwd_bwd(q, k, v, do, causal, scale)
+    rq, rk, rv = ref.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, scale)
+    errs = []
+    for got, want in ((dq, rq), (dk, rk), (dv, rv)):
+        g64 = to64(got)
+        errs.append(max(rel_fro(g64[b, h], want[b, h]) for b in range(B) for h in range(got.shape[1])))
+    record("bwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=1.0, deterministic=False,
+           dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2])
+    assert max(errs) <= GRAD_RTOL, errs
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_bwd_ragged_gqa(det):
+    check_full(2, 8, 2, 700, 128, True, seed=23, deterministic=det)
+
+
 def test_bwd_stress_rescale_inputs():
     check_full(1, 4, 4, 1024, 128, True, seed=19, qk_mult=4.0)
 
@@ -101,7 +127,7 @@ def test_bwd_workspace_checks():
     assert fa.fa_bwd(*args, ws, need - 256) == fa.FA_ERR_WORKSPACE
     assert fa.fa_bwd(*args, None, need) == fa.FA_ERR_WORKSPACE
     assert fa.fa_bwd(*args, ws, need) == fa.FA_OK
-    bad = (q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, 200, d, 0, d ** -0.5, 0)
+    bad = (q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, 96, 0, d ** -0.5, 0)
     assert fa.fa_bwd(*bad, ws, need) == fa.FA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
 
