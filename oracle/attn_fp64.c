@@ -36,7 +36,11 @@
  * Layouts (all fp64, row-major, contiguous):
  *   q, o, dout, dq : [B][H][Nq][d]      k, v, dk, dv : [B][Hkv][Nk][d]
  *   lse            : [B][H][Nq]
- * Causal masking is top-left aligned: query position p sees keys 0..p.
+ * Causal masking: query row i sits at position pos(i) and sees keys 0..pos(i).
+ * With Nq = Nk, pos(i) = i.  With Nq != Nk the plain reading for a block of
+ * queries that follows earlier keys (a KV cache) is bottom-right alignment,
+ * pos(i) = i + (Nk - Nq): the last query sees every key.  A row whose pos is
+ * negative sees no key; its O is 0 and its LSE -inf (no gradient flows).
  *
  * Return value: 0 on success, -1 on an invalid argument, -2 on out-of-memory.
  */
@@ -134,17 +138,18 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v,
     return oom ? -2 : 0;
 }
 
-/* Backward.  Query and key positions are 0..Nq-1 and 0..Nk-1.
- * Two plain passes, both straight from the formulas in the header:
+/* Backward.  Query row i sits at position i + qoff (see the causal note in the
+ * header), keys at 0..Nk-1.  Two plain passes, both straight from the formulas
+ * in the header:
  *  pass 1 (one query row at a time): P_i., dP_i., D_i, dS_i., dQ_i, and LSE_i;
  *  pass 2 (one key row j of a K/V head at a time): the column sums
  *         dV_j = sum_{h in group, i} P_ij dO_i and dK_j = scale sum dS_ij q_i,
  *         with P_ij = exp(S_ij - LSE_i) (the softmax written with its
  *         normaliser) and dS_ij formed exactly as in pass 1. */
-int oracle_attn_bwd(const double* q, const double* k, const double* v,
-                    const double* dout, double* dq, double* dk, double* dv,
-                    int B, int H, int Hkv, int Nq, int Nk, int d,
-                    int causal, double scale)
+int oracle_attn_bwd_off(const double* q, const double* k, const double* v,
+                        const double* dout, double* dq, double* dk, double* dv,
+                        int B, int H, int Hkv, int Nq, int Nk, int d,
+                        int causal, double scale, long long qoff)
 {
     if (check_args(B, H, Hkv, Nq, Nk, d)) return -1;
     const int group = H / Hkv;
@@ -179,7 +184,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v,
 
             double m = -INFINITY;
             for (int j = 0; j < Nk; ++j) {
-                double s = (causal && j > i) ? -INFINITY : scale * dot(qi, K + (long long)j * d, d);
+                double s = (causal && j > i + qoff) ? -INFINITY : scale * dot(qi, K + (long long)j * d, d);
                 p[j] = s;
                 if (s > m) m = s;
             }
@@ -219,7 +224,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v,
                 const int h = g * group + hh;
                 const long long base = ((long long)b * H + h) * Nq;
                 for (int i = 0; i < Nq; ++i) {
-                    if (causal && j > i) continue;
+                    if (causal && j > i + qoff) continue;
                     const long long ri = base + i;
                     if (lse[ri] == -INFINITY) continue;
                     const double* qi = q + ri * d;
@@ -240,4 +245,13 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v,
     free(lse);
     free(Dv);
     return oom ? -2 : 0;
+}
+
+/* Backward with the positions of the Nq = Nk case (qoff = 0). */
+int oracle_attn_bwd(const double* q, const double* k, const double* v,
+                    const double* dout, double* dq, double* dk, double* dv,
+                    int B, int H, int Hkv, int Nq, int Nk, int d,
+                    int causal, double scale)
+{
+    return oracle_attn_bwd_off(q, k, v, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale, 0);
 }

@@ -11,7 +11,8 @@ mistake in that shortcut would show up as a disagreement:
 
     dS_ij = sum_j' dP_ij' * P_ij' * (delta_jj' - P_ij)
 
-Inputs are nested lists ``x[b][h][n][c]``.
+Inputs are nested lists ``x[b][h][n][c]``.  For the causal mask query row i
+sits at position i + qoff (bottom-right alignment for Nq != Nk: qoff = Nk - Nq).
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ def _shape(x):
     return len(x), len(x[0]), len(x[0][0]), len(x[0][0][0])
 
 
-def fwd(q, k, v, causal, scale):
+def fwd(q, k, v, causal, scale, qoff=0):
     B, H, N, d = _shape(q)
     _, Hkv, Nk, _ = _shape(k)
     grp = H // Hkv
@@ -34,11 +35,14 @@ def fwd(q, k, v, causal, scale):
             for i in range(N):
                 s = []
                 for j in range(Nk):
-                    if causal and j > i:
+                    if causal and j > i + qoff:
                         s.append(-math.inf)
                     else:
                         s.append(scale * sum(q[b][h][i][c] * k[b][g][j][c] for c in range(d)))
-                m = max(s)
+                m = max(s) if s else -math.inf
+                if m == -math.inf:  # the row sees no key: O = 0, LSE = -inf
+                    lse[b][h][i] = -math.inf
+                    continue
                 e = [math.exp(x - m) if x != -math.inf else 0.0 for x in s]
                 z = sum(e)
                 for c in range(d):
@@ -47,7 +51,7 @@ def fwd(q, k, v, causal, scale):
     return o, lse
 
 
-def bwd(q, k, v, do, causal, scale):
+def bwd(q, k, v, do, causal, scale, qoff=0):
     B, H, N, d = _shape(q)
     _, Hkv, Nk, _ = _shape(k)
     grp = H // Hkv
@@ -60,11 +64,13 @@ def bwd(q, k, v, do, causal, scale):
             for i in range(N):
                 s = []
                 for j in range(Nk):
-                    if causal and j > i:
+                    if causal and j > i + qoff:
                         s.append(-math.inf)
                     else:
                         s.append(scale * sum(q[b][h][i][c] * k[b][g][j][c] for c in range(d)))
-                m = max(s)
+                m = max(s) if s else -math.inf
+                if m == -math.inf:  # the row sees no key: no gradient
+                    continue
                 e = [math.exp(x - m) if x != -math.inf else 0.0 for x in s]
                 z = sum(e)
                 p = [x / z for x in e]

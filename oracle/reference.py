@@ -50,6 +50,8 @@ def _load():
             lib.oracle_attn_fwd.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 7 + [ctypes.c_double]
             lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd_off.argtypes = [dp] * 7 + [ctypes.c_int] * 7 + [ctypes.c_double, ctypes.c_longlong]
+            lib.oracle_attn_bwd_off.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -94,11 +96,13 @@ def attn_fwd(q, k, v, causal: bool, scale: float, qpos=None):
     return o, lse
 
 
-def attn_bwd(q, k, v, dout, causal: bool, scale: float):
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, qoff: int = 0):
     """Analytic attention backward in fp64 for L = sum(O * dout).
 
     Returns (dq [B,H,Nq,d], dk [B,Hkv,Nk,d], dv [B,Hkv,Nk,d]); dk/dv of a
-    grouped K/V head are summed over the query heads that share it.
+    grouped K/V head are summed over the query heads that share it.  For the
+    causal mask, query row i sits at position i + qoff (qoff = Nk - Nq is the
+    bottom-right alignment of a query block that follows earlier keys).
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, H, Nq, d = q.shape
@@ -107,8 +111,8 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float):
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
-    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 B, H, Hkv, Nq, Nk, d, int(bool(causal)), float(scale))
+    rc = _load().oracle_attn_bwd_off(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     B, H, Hkv, Nq, Nk, d, int(bool(causal)), float(scale), int(qoff))
     if rc != 0:
         raise ValueError("oracle_attn_bwd failed with code %d" % rc)
     return dq, dk, dv

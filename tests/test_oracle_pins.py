@@ -263,3 +263,94 @@ def test_torch_sdpa_float64(causal):
     if causal:
         s = s.masked_fill(torch.ones(19, 19, dtype=torch.bool).triu(1), float("-inf"))
     np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+# ---- Nq != Nk: the causal mask places query row i at position i + qoff, qoff = Nk - Nq
+# (bottom-right alignment: the query block follows Nk - Nq earlier keys).
+
+QK_SHAPES = [
+    # B, H, Hkv, Nq, d, Nk
+    (1, 2, 1, 3, 3, 7),    # fewer queries than keys (a KV cache in front)
+    (1, 2, 2, 6, 2, 4),    # more queries than keys: the first two rows see no key
+    (2, 4, 2, 1, 4, 9),    # one query (decode)
+]
+
+
+@pytest.mark.parametrize("shape", QK_SHAPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_qk(shape, causal):
+    B, H, Hkv, Nq, d, Nk = shape
+    q, k, v, do = _case(11, B, H, Hkv, Nq, d, Nk)
+    qoff = Nk - Nq
+    scale = 0.7
+    o, lse = ref.attn_fwd(q, k, v, causal, scale, qpos=np.arange(Nq) + qoff)
+    ob, lseb = brute.fwd(q.tolist(), k.tolist(), v.tolist(), causal, scale, qoff)
+    np.testing.assert_allclose(o, np.array(ob), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isinf(lse), np.isinf(np.array(lseb)))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse[fin], np.array(lseb)[fin], rtol=0, atol=1e-12)
+    dq, dk, dv = ref.attn_bwd(q, k, v, do, causal, scale, qoff)
+    dqb, dkb, dvb = brute.bwd(q.tolist(), k.tolist(), v.tolist(), do.tolist(), causal, scale, qoff)
+    np.testing.assert_allclose(dq, np.array(dqb), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, np.array(dkb), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, np.array(dvb), rtol=0, atol=1e-11)
+
+
+def test_bottom_right_special_cases():
+    # one query at the end of the sequence sees every key: causal equals non-causal
+    q, k, v, do = _case(12, 1, 2, 1, 1, 4, 11)
+    qoff = 10
+    oc, lc = ref.attn_fwd(q, k, v, True, 0.5, qpos=np.arange(1) + qoff)
+    on, ln = ref.attn_fwd(q, k, v, False, 0.5)
+    np.testing.assert_allclose(oc, on, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lc, ln, rtol=0, atol=1e-14)
+    gc = ref.attn_bwd(q, k, v, do, True, 0.5, qoff)
+    gn = ref.attn_bwd(q, k, v, do, False, 0.5)
+    for a, b in zip(gc, gn):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    # with qoff = 0 the offset backward is the square causal backward
+    q, k, v, do = _case(13, 1, 2, 2, 9, 3)
+    for a, b in zip(ref.attn_bwd(q, k, v, do, True, 0.4, 0), ref.attn_bwd(q, k, v, do, True, 0.4)):
+        np.testing.assert_array_equal(a, b)
+    # more queries than keys: rows with i + qoff < 0 see nothing (O = 0, LSE = -inf, dQ = 0)
+    # and contribute nothing to dK, dV; the remaining rows equal a square problem on the
+    # last Nk queries
+    q, k, v, do = _case(14, 1, 2, 1, 7, 3, 4)
+    qoff = 4 - 7
+    o, lse = ref.attn_fwd(q, k, v, True, 0.6, qpos=np.arange(7) + qoff)
+    dq, dk, dv = ref.attn_bwd(q, k, v, do, True, 0.6, qoff)
+    assert np.all(o[:, :, :3] == 0) and np.all(np.isneginf(lse[:, :, :3])) and np.all(dq[:, :, :3] == 0)
+    o2, lse2 = ref.attn_fwd(q[:, :, 3:], k, v, True, 0.6)
+    dq2, dk2, dv2 = ref.attn_bwd(q[:, :, 3:], k, v, do[:, :, 3:], True, 0.6)
+    np.testing.assert_allclose(o[:, :, 3:], o2, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[:, :, 3:], lse2, rtol=0, atol=1e-14)
+    for a, b in ((dq[:, :, 3:], dq2), (dk, dk2), (dv, dv2)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+
+
+def test_finite_differences_qk():
+    q, k, v, do = _case(15, 1, 2, 1, 4, 3, 9)
+    qoff = 5
+    scale = 0.8
+    dq, dk, dv = ref.attn_bwd(q, k, v, do, True, scale, qoff)
+    pos = np.arange(4) + qoff
+
+    def loss(qq, kk, vv):
+        o, _ = ref.attn_fwd(qq, kk, vv, True, scale, qpos=pos)
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp = x.copy()
+            xp[idx] += h
+            xm = x.copy()
+            xm[idx] -= h
+            plus = {"q": q, "k": k, "v": v}
+            minus = dict(plus)
+            plus[name] = xp
+            minus[name] = xm
+            fd[idx] = (loss(plus["q"], plus["k"], plus["v"]) - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-30)
+        assert err < 1e-6, (name, err)
