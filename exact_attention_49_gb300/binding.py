@@ -36,7 +36,10 @@ _S = ctypes.c_size_t
 
 _SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_fwd_qk": (_I, [_P] * 5 + [_I] * 7 + [_F, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd_qk_workspace_bytes": (_S, [_I] * 7),
+    "fa_bwd_qk": (_I, [_P] * 9 + [_I] * 7 + [_F, _I, _P, _S, _P]),
     "fa_bwd": (_I, [_P] * 9 + [_I] * 6 + [_F, _I, _P, _S, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_main": (_I, [_P] * 7 + [_I] * 6 + [_F, _I, _P, _S, _P]),
@@ -103,6 +106,22 @@ def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream=None) -> int:
                         int(causal), float(scale), _stream(stream))
 
 
+def fa_fwd_qk(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, stream=None) -> int:
+    return lib().fa_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk, d,
+                           int(causal), float(scale), _stream(stream))
+
+
+def fa_bwd_qk_workspace_bytes(B, H, Hkv, Nq, Nk, d, deterministic) -> int:
+    return int(lib().fa_bwd_qk_workspace_bytes(B, H, Hkv, Nq, Nk, d, int(deterministic)))
+
+
+def fa_bwd_qk(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale, deterministic,
+              workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_bwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, H, Hkv, Nq, Nk, d, int(causal), float(scale), int(deterministic),
+                           _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def fa_bwd_workspace_bytes(B, H, Hkv, N, d, deterministic) -> int:
     return int(lib().fa_bwd_workspace_bytes(B, H, Hkv, N, d, int(deterministic)))
 
@@ -160,20 +179,21 @@ def _check(fn, st):
 
 
 def _dims(q, k):
-    B, H, N, d = q.shape
+    B, H, Nq, d = q.shape
     Bk, Hkv, Nk, dk = k.shape
-    if Bk != B or Nk != N or dk != d:
+    if Bk != B or dk != d:
         raise ValueError("shape mismatch: q %s k %s" % (tuple(q.shape), tuple(k.shape)))
-    return B, H, Hkv, N, d
+    return B, H, Hkv, Nq, Nk, d
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
                       stream=None):
-    """Exact attention forward on CUDA bf16 tensors q [B,H,N,d], k/v [B,Hkv,N,d].
+    """Exact attention forward on CUDA bf16 tensors q [B,H,Nq,d], k/v [B,Hkv,Nk,d].
 
-    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]).  With Nq != Nk a causal mask is
+    aligned bottom-right (query row i sees keys 0..i + Nk - Nq)."""
     import torch
-    B, H, Hkv, N, d = _dims(q, k)
+    B, H, Hkv, N, Nk, d = _dims(q, k)
     for t in (q, k, v):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors")
@@ -183,7 +203,10 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check("fa_fwd", fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, causal, scale, stream))
+    if Nk == N:
+        _check("fa_fwd", fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, causal, scale, stream))
+    else:
+        _check("fa_fwd_qk", fa_fwd_qk(q, k, v, out, lse, B, H, Hkv, N, Nk, d, causal, scale, stream))
     return out, lse
 
 
@@ -192,16 +215,20 @@ def attention_backward(q, k, v, o, do, lse, causal: bool = False, scale: float |
                        stream=None):
     """Exact attention backward; returns (dq, dk, dv) as bf16 tensors."""
     import torch
-    B, H, Hkv, N, d = _dims(q, k)
+    B, H, Hkv, N, Nk, d = _dims(q, k)
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = fa_bwd_workspace_bytes(B, H, Hkv, N, d, deterministic)
+    ws_bytes = fa_bwd_qk_workspace_bytes(B, H, Hkv, N, Nk, d, deterministic)
     if workspace is None:
         # torch's caching allocator returns blocks aligned to at least 512 bytes
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
-    _check("fa_bwd", fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
-                            deterministic, workspace, workspace.numel(), stream))
+    if Nk == N:
+        _check("fa_bwd", fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                                deterministic, workspace, workspace.numel(), stream))
+    else:
+        _check("fa_bwd_qk", fa_bwd_qk(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, Nk, d, causal, scale,
+                                      deterministic, workspace, workspace.numel(), stream))
     return dq, dk, dv

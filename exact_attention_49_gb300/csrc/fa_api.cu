@@ -179,21 +179,26 @@ int fa_last_device_status(void* stream) {
   return v;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
-           int causal, float scale, void* stream) {
-  int st = check_shape(B, H, Hkv, N, d);
+int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+              int Nk, int d, int causal, float scale, void* stream) {
+  int st = check_shape(B, H, Hkv, Nq, d);
   if (st) return st;
+  if ((st = check_shape(B, H, Hkv, Nk, d))) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_scale(scale))) return st;
-  if (B == 0 || N == 0) return FA_OK;
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Nq == 0) return FA_OK;
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
+  if (Nk == 0) {  // no key: O = 0, LSE = -inf
+    cudaError_t e = launch_fwd_no_keys(o, lse, (long long)B * H * Nq, d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd (no keys) launch", e);
+  }
 
   CUtensorMap tq, tk, tv;
-  if (make_tmap_bf16_rows(&tq, q, d, N, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, N, (long long)B * Hkv) ||
-      make_tmap_bf16_rows(&tv, v, d, N, (long long)B * Hkv))
+  if (make_tmap_bf16_rows(&tq, q, d, Nq, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, Nk, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tv, v, d, Nk, (long long)B * Hkv))
     return FA_ERR_CUDA;
   FwdParams p{};
   p.o = o;
@@ -201,7 +206,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
-  p.N = N;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.qoff = Nk - Nq;
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.tau = options().rescale_threshold;
@@ -213,13 +220,18 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 
-// Workspace layout, with the rows of every head padded to Np = N rounded up to 128:
-// [dQ accumulator fp32 B*H*Np*d][lse2 fp32 B*H*Np][D fp32 B*H*Np][counters int32 B*H*Np/128]
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+           int causal, float scale, void* stream) {
+  return fa_fwd_qk(q, k, v, o, lse, B, H, Hkv, N, N, d, causal, scale, stream);
+}
+
+// Workspace layout, with the query rows of every head padded to Nqp = Nq rounded up to 128:
+// [dQ accumulator fp32 B*H*Nqp*d][lse2 fp32 B*H*Nqp][D fp32 B*H*Nqp][counters int32 B*H*Nqp/128]
 struct BwdWorkspace {
   size_t off_lse2, off_d, off_cnt, total;
 };
-static BwdWorkspace bwd_ws_layout(int B, int H, int N, int d, int deterministic) {
-  const size_t Np = ((size_t)N + 127) / 128 * 128;
+static BwdWorkspace bwd_ws_layout(int B, int H, int Nq, int d, int deterministic) {
+  const size_t Np = ((size_t)Nq + 127) / 128 * 128;
   const size_t rows = (size_t)B * H * Np;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdWorkspace w;
@@ -230,24 +242,80 @@ static BwdWorkspace bwd_ws_layout(int B, int H, int N, int d, int deterministic)
   return w;
 }
 
-size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic) {
-  if (check_shape(B, H, Hkv, N, d)) return 0;
+size_t fa_bwd_qk_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int deterministic) {
+  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d)) return 0;
   if (deterministic != 0 && deterministic != 1) return 0;
-  return bwd_ws_layout(B, H, N, d, deterministic).total;
+  return bwd_ws_layout(B, H, Nq, d, deterministic).total;
 }
 
-// Checks shared by the three backward stages; returns FA_OK when there is work to launch,
-// 1 when the problem is empty (nothing to do), or an error status.
-static int check_bwd_common(int B, int H, int Hkv, int N, int d, int deterministic, const void* ws,
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic) {
+  return fa_bwd_qk_workspace_bytes(B, H, Hkv, N, N, d, deterministic);
+}
+
+// Checks shared by the backward stages; returns FA_OK when there is work to launch,
+// 1 when there is no query row (nothing to do in the stages), or an error status.
+static int check_bwd_common(int B, int H, int Hkv, int Nq, int d, int deterministic, const void* ws,
                             size_t ws_bytes) {
-  int st = check_shape(B, H, Hkv, N, d);
+  int st = check_shape(B, H, Hkv, Nq, d);
   if (st) return st;
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
-  if (B == 0 || N == 0) return 1;
+  if (B == 0 || Nq == 0) return 1;
   if (!ws) return FA_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return FA_ERR_MISALIGNED;
-  if (ws_bytes < bwd_ws_layout(B, H, N, d, deterministic).total) return FA_ERR_WORKSPACE;
+  if (ws_bytes < bwd_ws_layout(B, H, Nq, d, deterministic).total) return FA_ERR_WORKSPACE;
   return FA_OK;
+}
+
+// The stages below assume their arguments were validated.
+static int bwd_pre_impl(const void* o, const void* dout, const float* lse, int B, int H, int Nq, int d,
+                        int deterministic, void* workspace, void* stream) {
+  const BwdWorkspace w = bwd_ws_layout(B, H, Nq, d, deterministic);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long heads = (long long)B * H;
+  cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float*>(ws + w.off_lse2),
+                                 reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws),
+                                 deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr, heads, Nq,
+                                 heads * ((Nq + 127) / 128), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
+}
+
+static int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv, int B,
+                         int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int deterministic,
+                         void* workspace, void* stream) {
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_tmap_bf16_rows(&tq, q, d, Nq, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, Nk, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tv, v, d, Nk, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tdo, dout, d, Nq, (long long)B * H))
+    return FA_ERR_CUDA;
+  const BwdWorkspace w = bwd_ws_layout(B, H, Nq, d, deterministic);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams p{};
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.lse2 = reinterpret_cast<const float*>(ws + w.off_lse2);
+  p.dvec = reinterpret_cast<const float*>(ws + w.off_d);
+  p.counters = deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.qoff = Nk - Nq;
+  p.causal = causal;
+  p.deterministic = deterministic;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale = scale;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_main launch", e);
+}
+
+static int bwd_post_impl(void* dq, int B, int H, int Nq, int d, void* workspace, void* stream) {
+  cudaError_t e = launch_bwd_post(static_cast<const float*>(workspace), dq, (long long)B * H, Nq, d,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_postprocess launch", e);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int Hkv, int N, int d,
@@ -258,14 +326,7 @@ int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, 
   if (!o || !dout || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
-  const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const long long heads = (long long)B * H;
-  cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float*>(ws + w.off_lse2),
-                                 reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws),
-                                 deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr, heads, N,
-                                 heads * ((N + 127) / 128), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
+  return bwd_pre_impl(o, dout, lse, B, H, N, d, deterministic, workspace, stream);
 }
 
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse, void* dk, void* dv,
@@ -282,32 +343,7 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
       !aligned(dv, 16))
     return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
-  CUtensorMap tq, tk, tv, tdo;
-  if (make_tmap_bf16_rows(&tq, q, d, N, (long long)B * H) || make_tmap_bf16_rows(&tk, k, d, N, (long long)B * Hkv) ||
-      make_tmap_bf16_rows(&tv, v, d, N, (long long)B * Hkv) ||
-      make_tmap_bf16_rows(&tdo, dout, d, N, (long long)B * H))
-    return FA_ERR_CUDA;
-  const BwdWorkspace w = bwd_ws_layout(B, H, N, d, deterministic);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  BwdParams p{};
-  p.dk = dk;
-  p.dv = dv;
-  p.dq_acc = reinterpret_cast<float*>(ws);
-  p.lse2 = reinterpret_cast<const float*>(ws + w.off_lse2);
-  p.dvec = reinterpret_cast<const float*>(ws + w.off_d);
-  p.counters = deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr;
-  p.B = B;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.N = N;
-  p.causal = causal;
-  p.deterministic = deterministic;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.scale = scale;
-  p.status = device_status_ptr();
-  if (!p.status) return FA_ERR_CUDA;
-  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_main launch", e);
+  return bwd_main_impl(q, k, v, dout, dk, dv, B, H, Hkv, N, N, d, causal, scale, deterministic, workspace, stream);
 }
 
 int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, int deterministic, void* workspace,
@@ -318,30 +354,52 @@ int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, int determ
   if (!dq) return FA_ERR_INVALID_ARG;
   if (!aligned(dq, 16)) return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
-  cudaError_t e = launch_bwd_post(static_cast<const float*>(workspace), dq, (long long)B * H, N, d,
-                                  static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_postprocess launch", e);
+  return bwd_post_impl(dq, B, H, N, d, workspace, stream);
+}
+
+int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate everything before the first launch
+  int st = check_shape(B, H, Hkv, Nk, d);
+  if (st) return st;
+  st = check_bwd_common(B, H, Hkv, Nq, d, deterministic, workspace, workspace_bytes);
+  if (st < 0) return st;
+  const bool no_queries = st == 1;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (B == 0 || (no_queries && Nk == 0)) return FA_OK;
+  if (!no_queries && (!q || !o || !dout || !lse || !dq)) return FA_ERR_INVALID_ARG;
+  if (Nk > 0 && (!k || !v || !dk || !dv)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (no_queries || Nk == 0) {
+    // no query row sees a key: the gradients that exist are zero
+    cudaError_t e = cudaSuccess;
+    if (no_queries) {
+      const size_t kv_bytes = (size_t)B * Hkv * Nk * d * 2;
+      e = cudaMemsetAsync(dk, 0, kv_bytes, s);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, s);
+    } else {
+      e = cudaMemsetAsync(dq, 0, (size_t)B * H * Nq * d * 2, s);
+    }
+    return e == cudaSuccess ? FA_OK : cuda_fail("cudaMemsetAsync", e);
+  }
+  st = bwd_pre_impl(o, dout, lse, B, H, Nq, d, deterministic, workspace, stream);
+  if (st) return st;
+  st = bwd_main_impl(q, k, v, dout, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale, deterministic, workspace, stream);
+  if (st) return st;
+  return bwd_post_impl(dq, B, H, Nq, d, workspace, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
            void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
            void* workspace, size_t workspace_bytes, void* stream) {
-  // validate everything before the first launch
-  int st = check_bwd_common(B, H, Hkv, N, d, deterministic, workspace, workspace_bytes);
-  if (st == 1) return FA_OK;
-  if (st) return st;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if ((st = check_scale(scale))) return st;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
-    return FA_ERR_MISALIGNED;
-  st = fa_bwd_preprocess(o, dout, lse, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
-  if (st) return st;
-  st = fa_bwd_main(q, k, v, dout, lse, dk, dv, B, H, Hkv, N, d, causal, scale, deterministic, workspace,
+  return fa_bwd_qk(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, N, d, causal, scale, deterministic, workspace,
                    workspace_bytes, stream);
-  if (st) return st;
-  return fa_bwd_postprocess(dq, B, H, Hkv, N, d, deterministic, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -111,9 +111,10 @@ __global__ void __launch_bounds__(512, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   // ---- work unit
-  const int N = p.N;
-  // Rows are padded per head to Np, a multiple of 128, in the workspace arrays (lse2, D,
-  // dQ accumulator); the last tiles of Q, dO, K, V read zeros past N (TMA out-of-bounds fill).
+  const int N = p.Nq;  // query rows; keys: p.Nk
+  // Query rows are padded per head to Np, a multiple of 128, in the workspace arrays (lse2, D,
+  // dQ accumulator); the last tiles of Q, dO (past Nq) and K, V (past Nk) read zeros (TMA
+  // out-of-bounds fill).
   const int Np = (N + 127) & ~127;
   const int nq = Np / 128;
   const int BG = p.B * p.Hkv;
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(512, 1)
   // accumulator lines, which stay in L2 (about 14% faster than key-tile-major order
   // over all heads on the B4 H16 N8192 workload).
   constexpr int kHeadGroup = 8;
-  const int nkv = Np / 128;
+  const int nkv = (p.Nk + 127) / 128;
   const int gi = blockIdx.x / (kHeadGroup * nkv);
   const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
   const int rem = blockIdx.x - gi * kHeadGroup * nkv;
@@ -130,8 +131,11 @@ __global__ void __launch_bounds__(512, 1)
   const int bg = gi * kHeadGroup + rem % gsz;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int grp = p.H / p.Hkv;
-  const int i0 = p.causal ? j : 0;
-  const int ni = nq - i0;
+  // causal: query row q sits at position q + qoff; the first query tile with a row at or after
+  // key 128 j is the first i with 128 i + 127 + qoff >= 128 j
+  const int first = 128 * j - 127 - p.qoff;
+  const int i0 = (p.causal && first > 0) ? (first + 127) / 128 : 0;
+  const int ni = max(nq - i0, 0);
   const int ntiles = grp * ni;
   auto tile_head = [&](int t) { return b * p.H + g * grp + t / ni; };  // b*H + h
   auto tile_row = [&](int t) { return i0 + t % ni; };                 // query tile index i
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 13) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && ntiles > 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
       for (int ch = 0; ch < C::CHUNKS; ++ch) {
         tma_load_3d(sbase + C::OFF_K + ch * 16384, &tm_k, kv_full, ch * 64, j * 128, bg);
@@ -226,7 +230,8 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
     auto sQ = [&](int s) { return sbase + C::OFF_Q + s * C::TILE; };
     auto sDO = [&](int s) { return sbase + C::OFF_DO + s * C::TILE; };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, p.status));
+    bool ok = ntiles > 0;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, p.status));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(st_full(0), 0, abort, p.status));
     if (ok) {
       tc_fence_after();
@@ -290,10 +295,12 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t scx2 = f2_pack(p.scale, p.scale);
     uint8_t* ds_row = smem + C::OFF_DS + w * 16384 + r * 128;
-    const bool key_pad = j * 128 + r >= N;
+    const bool key_pad = j * 128 + r >= p.Nk;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t & 1;
-      const bool diag = p.causal && tile_row(t) == j;
+      // causal: key 128 j + r is masked for query 128 i + 64 w + c when it lies after the
+      // query's position, i.e. for c < cut (cut <= 0: nothing masked in this half row)
+      const int cut = p.causal ? r + 128 * (j - tile_row(t)) - 64 * w - p.qoff : 0;
       // this half's 64 queries: lse2 and D, four per 16-byte shared load
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024) + 16 * w;
       const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024 + 512) + 16 * w;
@@ -321,14 +328,14 @@ __global__ void __launch_bounds__(512, 1)
           pv[4 * c4 + 3] = ex2_mufu(x23.y);
         }
       }
-      if (key_pad) {  // a key row past N (zero-filled K) carries no probability
+      if (key_pad) {  // a key row past Nk (zero-filled K) carries no probability
 #pragma unroll
         for (int c = 0; c < 64; ++c) pv[c] = 0.f;
       }
-      if (diag) {  // key r > query q is masked on the diagonal tile
+      if (cut > 0) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (r > 64 * w + c) pv[c] = 0.f;
+          if (c < cut) pv[c] = 0.f;
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -472,8 +479,8 @@ __global__ void __launch_bounds__(512, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
     if (ok) {
       tc_fence_after();
-      const size_t krow = (size_t)bg * N + (size_t)j * 128 + r;
-      const bool krow_valid = j * 128 + r < N;  // the last key tile may run past N
+      const size_t krow = (size_t)bg * p.Nk + (size_t)j * 128 + r;
+      const bool krow_valid = j * 128 + r < p.Nk;  // the last key tile may run past Nk
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which ? p.dk : p.dv) + krow * D);
@@ -482,6 +489,10 @@ __global__ void __launch_bounds__(512, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tcol + 32 * c, v);
+          if (ntiles == 0) {  // no query row sees these keys: their gradients are zero
+#pragma unroll
+            for (int m = 0; m < 32; ++m) v[m] = 0u;
+          }
 #pragma unroll
           for (int m = 0; m < 4; ++m)
             if (krow_valid)
@@ -637,7 +648,7 @@ static cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)((p.N + 127) / 128) * p.B * p.Hkv;
+  const long long blocks = (long long)((p.Nk + 127) / 128) * p.B * p.Hkv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   bwd_main_kernel<D><<<dim3((unsigned)blocks), dim3(512), C::SMEM, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();

@@ -23,6 +23,8 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; P (bf16) overwrites the first
 // half of its S block and feeds the PV MMA straight from TMEM.
 // Shared memory: Q0, Q1 and a ring of K/V tiles (K_j and V_j take turns).
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
 
   // ---- work unit: (b, h, block of 256 query rows); causal: heaviest blocks first
-  const int N = p.N;
+  const int N = p.Nq;  // query rows; keys: p.Nk
   const int ncb = (N + 255) / 256;
   const int BH = p.B * p.H;
   const int t = blockIdx.x;
@@ -79,8 +81,11 @@ __global__ void __launch_bounds__(320, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int g = h / (p.H / p.Hkv);
   const int q0 = cb * 256;
-  const int n_kv_all = (N + 127) / 128;
-  const int n_kv = p.causal ? min(n_kv_all, (q0 + 256) / 128) : n_kv_all;
+  const int n_kv_all = (p.Nk + 127) / 128;
+  // causal: the block's last row (position row + qoff) bounds the key tiles it needs; a block
+  // whose rows see no key at all still runs one fully masked tile (O = 0, LSE = -inf)
+  const int k_last = min(q0 + 255, N - 1) + p.qoff;
+  const int n_kv = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
   const int kv_z = b * p.Hkv + g;
 
   if (warp == 0 && lane == 0) {
@@ -236,11 +241,11 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
       }
       const int col0 = j * 128;
-      if ((p.causal && col0 + 127 > tile_row0) || col0 + 128 > N) {
+      if ((p.causal && col0 + 127 > tile_row0 + p.qoff) || col0 + 128 > p.Nk) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int col = col0 + c;
-          if ((p.causal && col > row) || col >= N) s[c] = -INFINITY;
+          if ((p.causal && col > row + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
         }
       }
       float mx4[4];
@@ -352,7 +357,7 @@ static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, c
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)((p.N + 255) / 256) * p.B * p.H;
+  const long long blocks = (long long)((p.Nq + 255) / 256) * p.B * p.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   fwd_kernel<D, POLY><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
@@ -375,6 +380,22 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdParams& p, int poly_cols, cudaStream_t stream) {
   if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, poly_cols, stream);
   return launch_fwd_d<128>(tq, tk, tv, p, poly_cols, stream);
+}
+
+// Attention over zero keys: O = 0 and LSE = -inf (the softmax has no term).
+__global__ void __launch_bounds__(256) fwd_no_keys_kernel(uint4* __restrict__ o, float* __restrict__ lse, long long n16,
+                                                          long long rows) {
+  const long long nthr = (long long)gridDim.x * blockDim.x;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n16; k += nthr) o[k] = make_uint4(0, 0, 0, 0);
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < rows; k += nthr) lse[k] = -INFINITY;
+}
+
+cudaError_t launch_fwd_no_keys(void* o, float* lse, long long rows, int d, cudaStream_t stream) {
+  const long long n16 = rows * d * 2 / 16;
+  const long long want = (std::max(n16, rows) + 255) / 256;
+  const int grid = (int)std::min<long long>(std::max<long long>(want, 1), 4096);
+  fwd_no_keys_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(o), lse, n16, rows);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

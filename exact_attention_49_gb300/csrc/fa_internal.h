@@ -17,9 +17,10 @@ struct Options {
 Options& options();
 
 struct FwdParams {
-  void* o;           // bf16 [B,H,N,d]
-  float* lse;        // fp32 [B,H,N], natural log
-  int B, H, Hkv, N;
+  void* o;           // bf16 [B,H,Nq,d]
+  float* lse;        // fp32 [B,H,Nq], natural log
+  int B, H, Hkv, Nq, Nk;
+  int qoff;          // causal: query row i sits at position i + qoff = i + Nk - Nq
   int causal;
   float scale_log2;  // softmax scale * log2(e)
   float tau;         // rescale threshold, log2 units
@@ -28,13 +29,14 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  void* dk;           // bf16 [B,Hkv,N,d]
-  void* dv;           // bf16 [B,Hkv,N,d]
-  float* dq_acc;      // fp32 [B,H,N,d] dQ accumulator (workspace)
-  const float* lse2;  // per query row LSE * log2(e) (workspace)
-  const float* dvec;  // per query row D = sum_c dO_c O_c (workspace)
-  int* counters;      // deterministic mode: [B*H*(N/128)] ordering counters (workspace)
-  int B, H, Hkv, N;
+  void* dk;           // bf16 [B,Hkv,Nk,d]
+  void* dv;           // bf16 [B,Hkv,Nk,d]
+  float* dq_acc;      // fp32 [B,H,Nqp,d] dQ accumulator, rows padded to Nqp = Nq rounded up to 128 (workspace)
+  const float* lse2;  // per padded query row LSE * log2(e) (workspace)
+  const float* dvec;  // per padded query row D = sum_c dO_c O_c (workspace)
+  int* counters;      // deterministic mode: [B*H*(Nqp/128)] ordering counters (workspace)
+  int B, H, Hkv, Nq, Nk;
+  int qoff;           // causal: query row i sits at position i + qoff = i + Nk - Nq
   int causal;
   int deterministic;
   float scale_log2;   // softmax scale * log2(e)
@@ -48,6 +50,8 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
+// O = 0 and LSE = -inf for every query row (attention over zero keys)
+cudaError_t launch_fwd_no_keys(void* o, float* lse, long long rows, int d, cudaStream_t stream);
 
 // Launch the forward kernel for head dim d (64 or 128) with poly_cols of every 32
 // exponentials on the FMA polynomial (0, 4, 8, 12 or 16).  Returns a cudaError_t.

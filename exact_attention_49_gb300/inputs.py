@@ -52,13 +52,14 @@ def long_context(N: int, d: int) -> Workload:
                     seed=5, backward=False)
 
 
-def make_inputs(B: int, H: int, Hkv: int, N: int, d: int, seed: int, qk_mult: float = 1.0):
-    """Return bf16 CPU tensors (q, k, v, do): q/do [B,H,N,d], k/v [B,Hkv,N,d]."""
+def make_inputs(B: int, H: int, Hkv: int, N: int, d: int, seed: int, qk_mult: float = 1.0, Nk: int | None = None):
+    """Return bf16 CPU tensors (q, k, v, do): q/do [B,H,N,d], k/v [B,Hkv,Nk,d] (Nk = N by default)."""
+    Nk = N if Nk is None else Nk
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     q = torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    k = torch.randn((B, Hkv, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn((B, Hkv, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
     do = torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
     if qk_mult != 1.0:
         q = q * qk_mult

@@ -68,6 +68,17 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
 
+/* Forward with different query and key lengths: q, o [B,H,Nq,d], lse
+ * [B,H,Nq]; k, v [B,Hkv,Nk,d].  causal = 1 aligns the mask bottom-right:
+ * query row i sits at position i + (Nk - Nq) and sees keys 0..i + Nk - Nq,
+ * so a block of Nq new queries after Nk - Nq cached keys (or one decoding
+ * query, Nq = 1) sees every earlier key.  The pages do not treat Nq != Nk;
+ * this is the plain reading for a query block that follows earlier keys.  A
+ * row that sees no key (Nq > Nk, i < Nq - Nk) gets O = 0 and LSE = -inf, as
+ * does every row when Nk = 0.  fa_fwd is fa_fwd_qk with Nq = Nk = N. */
+int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, void* stream);
+
 /* Bytes of device workspace fa_bwd needs, with the rows of every head padded
  * to Np = N rounded up to a multiple of 128: the fp32 dQ accumulator
  * [B,H,Np,d], one (LSE in log2 units, D) fp32 pair per padded query row, and
@@ -84,6 +95,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv,
            int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward with different query and key lengths (the mask of fa_fwd_qk):
+ * q, o, dout, dq [B,H,Nq,d], lse [B,H,Nq]; k, v, dk, dv [B,Hkv,Nk,d].  Rows
+ * that see no key get dQ = 0 and add nothing to dK, dV; keys no query sees
+ * get dK = dV = 0.  The workspace (256-byte aligned) must hold
+ * fa_bwd_qk_workspace_bytes(...) bytes; its size depends on Nq only.
+ * fa_bwd is fa_bwd_qk with Nq = Nk = N. */
+size_t fa_bwd_qk_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int deterministic);
+int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv,
+              int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int deterministic,
+              void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of fa_bwd, exposed so that callers (and the benchmark) can
  * time or schedule them separately; they must run in this order on one
