@@ -27,9 +27,12 @@
 // The dQ accumulation over key tiles is the only cross-CTA sum.  Default: fp32
 // vector reductions (red.global.add.v4.f32) in whatever order CTAs reach them.
 // Deterministic mode (FA4's deterministic backward, wiki 未解決の問い): the CTA
-// of key tile j waits (bounded) until the tiles 0..j-1 have added their part of
-// query tile i, then adds with plain loads and stores, so the summation order is
-// fixed and results are bit-identical from run to run.
+// of key tile j waits (bounded) until the key tiles ranked before it have added
+// their part of query tile i — tiles 0..j-1 in general, the tiles above j when
+// the mask is causal (descending order, see the work-unit mapping) — then adds
+// its part with the same reductions, fences them and releases the next tile: one
+// contributor at a time in a fixed order, so results are bit-identical from run
+// to run.
 //
 // Warp roles of the main kernel (512 threads, 16 warps):
 //   warps 0-3   compute, query columns 0-63 of each tile (thread = key row = TMEM lane)
@@ -127,7 +130,13 @@ __global__ void __launch_bounds__(512, 1)
   const int gi = blockIdx.x / (kHeadGroup * nkv);
   const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
   const int rem = blockIdx.x - gi * kHeadGroup * nkv;
-  const int j = rem / gsz;
+  // Deterministic causal mode adds the key tiles' dQ parts of a query tile in descending
+  // key-tile order and schedules the lightest key tiles first: the CTA of key tile j then
+  // waits only on key tiles above it, which started earlier and reach every query tile one
+  // step before it does, so no lag accumulates along the chain (ascending order makes tile
+  // j wait for tile j-1, which reaches the query tile one step later than j).
+  const bool desc = p.deterministic && p.causal;
+  const int j = desc ? nkv - 1 - rem / gsz : rem / gsz;
   const int bg = gi * kHeadGroup + rem % gsz;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int grp = p.H / p.Hkv;
@@ -398,11 +407,14 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) break;
       tc_fence_after();
       int* counter = p.deterministic ? p.counters + ((size_t)bh * nq + i) : nullptr;
+      // this key tile's place in the fixed order of query tile i's contributions: ascending
+      // j, or (deterministic causal) descending from the last key tile that query tile i sees
+      const int rank = desc ? min(nkv - 1, (128 * i + 127 + p.qoff) / 128) - j : j;
       if (p.deterministic) {
-        // wait for key tiles 0..j-1 to finish their part of this query tile
+        // wait for the contributions ranked before this one
         if (r == 0) {
           const uint64_t t0 = globaltimer();
-          while (ld_acquire(counter) != j) {
+          while (ld_acquire(counter) != rank) {
             if (*abort || globaltimer() - t0 > kWaitLimitNs) {
               *abort = 1;
               atomicCAS(p.status, 0, kStatusTimeout);
@@ -428,16 +440,14 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(dq_empty);
           }
           float* c0 = col + (size_t)(64 * half) * D;
-          if (!p.deterministic) {
+          // deterministic mode: this CTA is the only one adding to query tile i right now (the
+          // counter orders the contributions), so the reductions land in a fixed order too;
+          // after a timeout nothing is added
+          if (!p.deterministic || !*abort) {
 #pragma unroll
             for (int m = 0; m < 32; ++m) red_add(c0 + (size_t)m * D, __uint_as_float(va[m]));
 #pragma unroll
             for (int m = 0; m < 32; ++m) red_add(c0 + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
-          } else if (!*abort) {
-#pragma unroll
-            for (int m = 0; m < 32; ++m) c0[(size_t)m * D] += __uint_as_float(va[m]);
-#pragma unroll
-            for (int m = 0; m < 32; ++m) c0[(size_t)(32 + m) * D] += __uint_as_float(vb[m]);
           }
         }
       } else {
@@ -450,29 +460,18 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(dq_empty);
           }
-          if (!p.deterministic) {
+          if (!p.deterministic || !*abort) {  // ordered in deterministic mode, as above
 #pragma unroll
             for (int m = 0; m < 8; ++m)
               red_add_v4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
                          __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
-          } else if (!*abort) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * m);
-              float4 x = *a;
-              x.x += __uint_as_float(v[4 * m]);
-              x.y += __uint_as_float(v[4 * m + 1]);
-              x.z += __uint_as_float(v[4 * m + 2]);
-              x.w += __uint_as_float(v[4 * m + 3]);
-              *a = x;
-            }
           }
         }
       }
       if (p.deterministic) {
         __threadfence();
         named_bar(1, 128);
-        if (r == 0) st_release(counter, j + 1);
+        if (r == 0) st_release(counter, rank + 1);
       }
     }
     // mma_done is committed after every MMA of the CTA, the last dK one included
