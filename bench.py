@@ -401,6 +401,89 @@ def run_ours(args, w):
     return 0
 
 
+# Decoding workloads (split-KV forward, fa_fwd_splitkv): B, Hq, Hkv, Nq, Nk, d, causal.
+DECODE = {
+    "D1": ("D1 decode B8 Hq32 Hkv8 Nq1 Nk16384 d128 causal", 8, 32, 8, 1, 16384, 128),
+    "D2": ("D2 decode B8 Hq32 Hkv8 Nq1 Nk65536 d128 causal", 8, 32, 8, 1, 65536, 128),
+    "D3": ("D3 decode B32 Hq32 Hkv8 Nq1 Nk8192 d128 causal", 32, 32, 8, 1, 8192, 128),
+    "D4": ("D4 decode B8 Hq32 Hkv8 Nq4 Nk16384 d128 causal", 8, 32, 8, 4, 16384, 128),
+    "D5": ("D5 decode B8 Hq32 Hkv32 Nq1 Nk16384 d128 causal", 8, 32, 32, 1, 16384, 128),
+}
+
+
+def run_decode(args):
+    """Time the split-KV forward on a decoding workload: HBM-bound (K and V are streamed once
+    per K/V head), so the line reports the K/V bytes per second against the measured HBM
+    copy bandwidth.  L2 is flushed (a 256 MiB write) before every timed step."""
+    import torch
+    from exact_attention_49_gb300 import binding as fa
+    from exact_attention_49_gb300.inputs import make_inputs
+    name, B, H, Hkv, Nq, Nk, d = DECODE[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q, k, v, _ = make_inputs(B, H, Hkv, Nq, d, seed=7, Nk=Nk)
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_fwd_splitkv_workspace_bytes(B, H, Hkv, Nq, Nk, d, 0)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    scale = d ** -0.5
+
+    def split():
+        st = fa.fa_fwd_splitkv(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, 1, scale, 0, ws, ws_bytes, stream)
+        if st != fa.FA_OK:
+            raise fa.FAError("fa_fwd_splitkv", st)
+
+    def onepass():
+        st = fa.fa_fwd_qk(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, 1, scale, stream)
+        if st != fa.FA_OK:
+            raise fa.FAError("fa_fwd_qk", st)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        with ClockSampler(0) as clk:
+            for _ in range(steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts), clk.summary()
+
+    ms, clocks = timed(split, args.steps)
+    ms_one, _ = timed(onepass, max(3, args.steps // 3))
+    st = fa.fa_last_device_status()
+    if st != fa.FA_OK:
+        raise fa.FAError("device status after the timed steps", st)
+    kv_bytes = 2 * B * Hkv * Nk * d * 2
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    line = {
+        "metric": "decode K/V bytes streamed per second (bf16, 1×GB300)", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "Hq": H, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d, "causal": True,
+                   "l2": "256 MiB written before every timed step", "splits": "library choice",
+                   "kv_bytes_per_step": kv_bytes},
+        "roofline": {"bound": "hbm", "kernel": "fwd_kernel (split-KV) + fwd_combine_kernel", "achieved": gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                     "peak_source": ("measured hbm_gbs (MEASURED_PEAKS.json)" if src == "measured"
+                                     else "fallback 6.8 TB/s")},
+        "one_pass_forward_ms": ms_one, "speedup_vs_one_pass": ms_one / ms,
+        "gpu_launches": 2 * args.steps if ws_bytes > 0 else args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,6 +502,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in DECODE:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "decoding workloads are timed for the GPU path only"}))
+            return 0
+        return run_decode(args)
     from exact_attention_49_gb300.inputs import WORKLOADS, long_context
     w = long_context(args.seq, args.head_dim) if args.workload == "C5" else WORKLOADS[args.workload]
     if args.batch:

@@ -37,6 +37,8 @@ _S = ctypes.c_size_t
 _SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_fwd_qk": (_I, [_P] * 5 + [_I] * 7 + [_F, _P]),
+    "fa_fwd_splitkv_workspace_bytes": (_S, [_I] * 7),
+    "fa_fwd_splitkv": (_I, [_P] * 5 + [_I] * 7 + [_F, _I, _P, _S, _P]),
     "fa_bwd_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_qk_workspace_bytes": (_S, [_I] * 7),
     "fa_bwd_qk": (_I, [_P] * 9 + [_I] * 7 + [_F, _I, _P, _S, _P]),
@@ -109,6 +111,16 @@ def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream=None) -> int:
 def fa_fwd_qk(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, stream=None) -> int:
     return lib().fa_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk, d,
                            int(causal), float(scale), _stream(stream))
+
+
+def fa_fwd_splitkv_workspace_bytes(B, H, Hkv, Nq, Nk, d, splits) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_bytes(B, H, Hkv, Nq, Nk, d, int(splits)))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, splits, workspace, workspace_bytes,
+                   stream=None) -> int:
+    return lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk, d, int(causal),
+                                float(scale), int(splits), _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd_qk_workspace_bytes(B, H, Hkv, Nq, Nk, d, deterministic) -> int:
@@ -207,6 +219,28 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         _check("fa_fwd", fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, causal, scale, stream))
     else:
         _check("fa_fwd_qk", fa_fwd_qk(q, k, v, out, lse, B, H, Hkv, N, Nk, d, causal, scale, stream))
+    return out, lse
+
+
+def attention_decode(q, k, v, causal: bool = False, scale: float | None = None, splits: int = 0, out=None,
+                     lse=None, workspace=None, stream=None):
+    """Split-KV forward (few queries against many keys), same results as attention_forward.
+
+    q [B,H,Nq,d], k/v [B,Hkv,Nk,d] CUDA bf16; returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]).
+    ``splits`` = 0 lets the library choose the number of key-range splits."""
+    import torch
+    B, H, Hkv, N, Nk, d = _dims(q, k)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = fa_fwd_splitkv_workspace_bytes(B, H, Hkv, N, Nk, d, splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("fa_fwd_splitkv", fa_fwd_splitkv(q, k, v, out, lse, B, H, Hkv, N, Nk, d, causal, scale, splits,
+                                            workspace, 0 if workspace is None else workspace.numel(), stream))
     return out, lse
 
 

@@ -3,6 +3,7 @@
 // before any CUDA call, so a rejected call never touches the GPU.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -114,6 +115,15 @@ static int check_shape(int B, int H, int Hkv, int N, int d) {
 
 static int check_scale(float scale) { return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG; }
 
+// multiprocessors of the current device (148 if it cannot be read)
+static int sm_count_api() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      v <= 0)
+    return 148;
+  return v;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -213,11 +223,105 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.tau = options().rescale_threshold;
   p.drop_it = options().debug_drop_kv_load ? 2 : -1;
+  p.splits = 1;
+  p.split_tiles = (Nk + 127) / 128;
+  p.pos_mod = 0;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
+}
+
+// Split-KV forward for few queries against many keys (decoding).  The H/Hkv query heads of a
+// K/V group are contiguous in q, o and lse, so they are taken as one head of g*Nq rows (query
+// row i of head h becomes row (h % g) * Nq + i, at causal position i + Nk - Nq): K and V are
+// then read once per group.  The key tiles are split over `splits` CTAs per 256-row block.
+static int splitkv_choice(int B, int H, int Hkv, int Nq, int Nk, int splits) {
+  const int rows = (H / Hkv) * Nq;
+  const long long blocks = (long long)B * Hkv * ((rows + 255) / 256);
+  const int n_kv = (Nk + 127) / 128;
+  if (splits <= 0) {
+    // one CTA per SM at a time: minimise (waves) x (key tiles per CTA + a fixed cost of about
+    // two tiles for the CTA's prologue and epilogue)
+    const long long sms = sm_count_api();
+    long long best = -1;
+    for (int S = 1; S <= std::min(n_kv, 256); ++S) {
+      const long long waves = (blocks * S + sms - 1) / sms;
+      const long long cost = waves * ((n_kv + S - 1) / S + 2);
+      if (best < 0 || cost < best) {
+        best = cost;
+        splits = S;
+      }
+    }
+  }
+  return std::max(1, std::min(splits, std::max(1, n_kv)));
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int splits) {
+  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d) || splits < 0 || splits > 4096) return 0;
+  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, splits);
+  if (S == 1) return 0;
+  const size_t rows = (size_t)B * H * Nq;
+  return ((size_t)S * rows * d * 4 + 255) / 256 * 256 + (size_t)S * rows * 4;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+                   int Nk, int d, int causal, float scale, int splits, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int st = check_shape(B, H, Hkv, Nq, d);
+  if (st) return st;
+  if ((st = check_shape(B, H, Hkv, Nk, d))) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (splits < 0 || splits > 4096) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Nq == 0) return FA_OK;
+  if (Nk == 0) return fa_fwd_qk(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, stream);
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  const int g = H / Hkv;
+  if ((long long)g * Nq > (1 << 30)) return FA_ERR_INVALID_ARG;
+  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, splits);
+  const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, Hkv, Nq, Nk, d, splits);
+  if (S > 1) {
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  }
+  if ((st = check_device())) return st;
+  const int rows = g * Nq;  // per K/V head
+  CUtensorMap tq, tk, tv;
+  if (make_tmap_bf16_rows(&tq, q, d, rows, (long long)B * Hkv) || make_tmap_bf16_rows(&tk, k, d, Nk, (long long)B * Hkv) ||
+      make_tmap_bf16_rows(&tv, v, d, Nk, (long long)B * Hkv))
+    return FA_ERR_CUDA;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = Hkv;
+  p.Hkv = Hkv;
+  p.Nq = rows;
+  p.Nk = Nk;
+  p.qoff = Nk - Nq;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.tau = options().rescale_threshold;
+  p.drop_it = -1;
+  p.splits = S;
+  const int n_kv = (Nk + 127) / 128;
+  p.split_tiles = (n_kv + S - 1) / S;
+  p.pos_mod = Nq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t all_rows = (size_t)B * H * Nq;
+  p.o_part = S > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  p.lse_part = S > 1 ? reinterpret_cast<float*>(ws + ((size_t)S * all_rows * d * 4 + 255) / 256 * 256) : nullptr;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, s);
+  if (e == cudaSuccess && S > 1) e = launch_fwd_combine(d, p.o_part, p.lse_part, o, lse, S, (long long)all_rows, s);
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd_splitkv launch", e);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,

@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(320, 1)
   const int N = p.Nq;  // query rows; keys: p.Nk
   const int ncb = (N + 255) / 256;
   const int BH = p.B * p.H;
-  const int t = blockIdx.x;
+  const int sp = blockIdx.x % p.splits;  // key-range split (split-KV); 0 when splits = 1
+  const int t = blockIdx.x / p.splits;
   const int cb = p.causal ? (ncb - 1 - t / BH) : (t / BH);
   const int bh = t % BH;
   const int b = bh / p.H, h = bh % p.H;
@@ -84,8 +85,15 @@ __global__ void __launch_bounds__(320, 1)
   const int n_kv_all = (p.Nk + 127) / 128;
   // causal: the block's last row (position row + qoff) bounds the key tiles it needs; a block
   // whose rows see no key at all still runs one fully masked tile (O = 0, LSE = -inf)
-  const int k_last = min(q0 + 255, N - 1) + p.qoff;
-  const int n_kv = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
+  const int last_row = min(q0 + 255, N - 1);
+  const int k_last = (p.pos_mod ? min(last_row, p.pos_mod - 1) : last_row) + p.qoff;
+  const int n_vis = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
+  // this CTA's key tiles [j0, j0 + n_kv); a split whose range holds no visible key still runs
+  // one fully masked tile, which gives O = 0 and LSE = -inf for it
+  const int j0 = sp * p.split_tiles;
+  const int n_kv = max(1, min(n_vis, j0 + p.split_tiles) - j0);
+  // a block with at most 128 rows (a ragged last block; decoding) runs query tile 0 only
+  const bool two = N - q0 > 128;
   const int kv_z = b * p.Hkv + g;
 
   if (warp == 0 && lane == 0) {
@@ -132,7 +140,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_expect_tx(full_bar(slot), C::TILE);
         for (int ch = 0; ch < C::CHUNKS; ++ch)
           tma_load_3d(smem_u32(sRing + slot * C::TILE + ch * 16384), (it & 1) ? &tm_v : &tm_k, full_bar(slot),
-                      ch * 64, (it >> 1) * 128, kv_z);
+                      ch * 64, (j0 + (it >> 1)) * 128, kv_z);
         issued = it + 1;
       }
       if (*abort) {
@@ -180,8 +188,10 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         issue_s(0, slot_of(0));
         mma_commit(s_full(0));
-        issue_s(1, slot_of(0));
-        mma_commit(s_full(1));
+        if (two) {
+          issue_s(1, slot_of(0));
+          mma_commit(s_full(1));
+        }
         mma_commit(empty_bar(slot_of(0)));
       }
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -198,14 +208,18 @@ __global__ void __launch_bounds__(320, 1)
           issue_s(0, slot_of(itk));
           mma_commit(s_full(0));
         }
-        if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
-        tc_fence_after();
-        issue_pv(1, slot_of(itv), j > 0);
-        mma_commit(o_bar(1));
+        if (two) {
+          if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_pv(1, slot_of(itv), j > 0);
+          mma_commit(o_bar(1));
+        }
         mma_commit(empty_bar(slot_of(itv)));
         if (more) {
-          issue_s(1, slot_of(itk));
-          mma_commit(s_full(1));
+          if (two) {
+            issue_s(1, slot_of(itk));
+            mma_commit(s_full(1));
+          }
           mma_commit(empty_bar(slot_of(itk)));
         }
       }
@@ -216,8 +230,10 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int w = warp >> 2;            // query tile
+    if (w == 1 && !two) goto softmax_done;  // no row of this block falls in query tile 1
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
-    const int row = q0 + w * 128 + r;   // absolute query position
+    const int row = q0 + w * 128 + r;   // absolute query row
+    const int rpos = p.pos_mod ? row % p.pos_mod : row;  // its position for the causal mask
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + (w ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_off + (w ? C::COL_O1 : C::COL_O0);
@@ -240,12 +256,13 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
       }
-      const int col0 = j * 128;
-      if ((p.causal && col0 + 127 > tile_row0 + p.qoff) || col0 + 128 > p.Nk) {
+      const int col0 = (j0 + j) * 128;
+      // packed rows: the smallest position in the tile is 0 (+ qoff)
+      if ((p.causal && col0 + 127 > (p.pos_mod ? 0 : tile_row0) + p.qoff) || col0 + 128 > p.Nk) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int col = col0 + c;
-          if ((p.causal && col > row + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
+          if ((p.causal && col > rpos + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
         }
       }
       float mx4[4];
@@ -317,6 +334,22 @@ __global__ void __launch_bounds__(320, 1)
       const float2 le = f2_unpack(l_exact), lr = f2_unpack(l_round);
       const float l = le.x + le.y, lrs = lr.x + lr.y;
       const float inv_l = lrs > 0.f ? 1.f / lrs : 0.f;
+      if (p.splits > 1) {  // split-KV partial: fp32 O over this split's keys, LSE in log2 units
+        const size_t prow = ((size_t)sp * BH + bh) * N + row;
+        float4* op = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tO + 32 * c, rr);
+          if (row < N) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              op[c * 8 + v4] = make_float4(__uint_as_float(rr[4 * v4]) * inv_l, __uint_as_float(rr[4 * v4 + 1]) * inv_l,
+                                           __uint_as_float(rr[4 * v4 + 2]) * inv_l, __uint_as_float(rr[4 * v4 + 3]) * inv_l);
+          }
+        }
+        if (row < N) p.lse_part[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+      } else {
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * N + row) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -333,9 +366,11 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (row < N) p.lse[(size_t)bh * N + row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
     }
   }
 
+softmax_done:
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -357,7 +392,7 @@ static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, c
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)((p.Nq + 255) / 256) * p.B * p.H;
+  const long long blocks = (long long)((p.Nq + 255) / 256) * p.B * p.H * p.splits;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   fwd_kernel<D, POLY><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
@@ -380,6 +415,57 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdParams& p, int poly_cols, cudaStream_t stream) {
   if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, poly_cols, stream);
   return launch_fwd_d<128>(tq, tk, tv, p, poly_cols, stream);
+}
+
+// Split-KV merge, one warp per query row: with m = max_s lse_s (log2 units) and
+// w_s = 2^(lse_s - m), O = sum_s w_s o_s / sum_s w_s and LSE = ln 2 * (m + log2 sum_s w_s) —
+// the online-softmax merge of the splits' (max, sum, output) triples.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ o_part,
+                                                          const float* __restrict__ lse_part, uint16_t* __restrict__ o,
+                                                          float* __restrict__ lse, int S, long long rows) {
+  constexpr int PER = D / 32;  // fp32 elements per lane (4 or 2)
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  const int lane = threadIdx.x & 31;
+  for (long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); row < rows; row += nwarps) {
+    float m = -INFINITY;
+    for (int s = lane; s < S; s += 32) m = fmaxf(m, lse_part[(size_t)s * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float acc[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const float ls = lse_part[(size_t)s * rows + row];
+        const float wgt = ls == -INFINITY ? 0.f : exp2f(ls - m);
+        wsum += wgt;
+        const float* src = o_part + ((size_t)s * rows + row) * D + lane * PER;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[k] = fmaf(wgt, src[k], acc[k]);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint16_t* dst = o + row * D + lane * PER;
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) {
+      const uint32_t pk = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+      *reinterpret_cast<uint32_t*>(dst + k) = pk;
+    }
+    if (lane == 0) lse[row] = wsum > 0.f ? (m + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+cudaError_t launch_fwd_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse, int splits,
+                               long long rows, cudaStream_t stream) {
+  const long long want = (rows + 7) / 8;
+  const int grid = (int)std::min<long long>(std::max<long long>(want, 1), 4096);
+  if (d == 64)
+    fwd_combine_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o), lse, splits, rows);
+  else
+    fwd_combine_kernel<128><<<grid, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o), lse, splits, rows);
+  return cudaGetLastError();
 }
 
 // Attention over zero keys: O = 0 and LSE = -inf (the softmax has no term).

@@ -26,6 +26,15 @@ struct FwdParams {
   float tau;         // rescale threshold, log2 units
   int* status;       // device status word
   int drop_it;       // failure-injection test hook: K/V load index the producer skips (-1: none)
+  // split-KV (decode): the key tiles are divided among `splits` CTAs per query block, each
+  // writing an fp32 partial O (normalised over its keys) and its LSE (log2 units); a combine
+  // kernel merges them.  splits = 1 is the plain forward (bf16 O, natural-log LSE).
+  int splits;
+  int split_tiles;   // key tiles per split
+  int pos_mod;       // causal: row r sits at position (r % pos_mod) + qoff (query heads packed
+                     // as rows, pos_mod = Nq); 0: position r + qoff
+  float* o_part;     // splits > 1: fp32 [splits][B*H][Nq][d]
+  float* lse_part;   // splits > 1: fp32 [splits][B*H][Nq]
 };
 
 struct BwdParams {
@@ -50,6 +59,9 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
+// Merge split-KV partials: LSE = log sum_s 2^lse_s, O = sum_s 2^(lse_s - LSE) o_s (bf16)
+cudaError_t launch_fwd_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse, int splits,
+                               long long rows, cudaStream_t stream);
 // O = 0 and LSE = -inf for every query row (attention over zero keys)
 cudaError_t launch_fwd_no_keys(void* o, float* lse, long long rows, int d, cudaStream_t stream);
 

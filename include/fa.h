@@ -79,6 +79,23 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
               int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, void* stream);
 
+/* Split-KV forward for decoding (few queries, many keys); same inputs,
+ * outputs and mask as fa_fwd_qk.  The H/Hkv query heads that share a K/V head
+ * are processed together as one block of rows, so K and V are read once per
+ * group, and the keys are divided among `splits` CTAs per block (0 = choose:
+ * about two CTAs per SM).  Each split writes an fp32 partial O, normalised
+ * over its keys, and its LSE into the workspace; a second kernel merges them
+ * with the online-softmax rule (the running-max rescaling of the explainer's
+ * online-softmax paragraph applied to whole splits): LSE = log sum_s e^LSE_s,
+ * O = sum_s e^(LSE_s - LSE) O_s.  The pages describe no decoding kernel; this
+ * is the merge of independent partial softmaxes that the online softmax
+ * implies.  Workspace: fa_fwd_splitkv_workspace_bytes(...) bytes, 256-byte
+ * aligned (0 bytes, and a null workspace allowed, when one split is chosen). */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int splits);
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int splits,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace fa_bwd needs, with the rows of every head padded
  * to Np = N rounded up to a multiple of 128: the fp32 dQ accumulator
  * [B,H,Np,d], one (LSE in log2 units, D) fp32 pair per padded query row, and
