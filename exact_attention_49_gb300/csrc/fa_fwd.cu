@@ -24,6 +24,7 @@
 // half of its S block and feeds the PV MMA straight from TMEM.
 // Shared memory: Q0, Q1 and a ring of K/V tiles (K_j and V_j take turns).
 #include <algorithm>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "sm103.cuh"
@@ -182,47 +183,56 @@ __global__ void __launch_bounds__(320, 1)
       };
       auto slot_of = [&](int it) { return it % C::STAGES; };
       auto par_of = [&](int it) { return (uint32_t)((it / C::STAGES) & 1); };
-      bool ok = mbar_wait(q_full, 0, abort, p.status);
-      if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), abort, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, slot_of(0));
-        mma_commit(s_full(0));
-        if (two) {
-          issue_s(1, slot_of(0));
-          mma_commit(s_full(1));
-        }
-        mma_commit(empty_bar(slot_of(0)));
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int itv = 2 * j + 1, itk = 2 * j + 2;
-        if (!(ok = mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status))) break;
-        if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
-        tc_fence_after();
-        issue_pv(0, slot_of(itv), j > 0);
-        mma_commit(o_bar(0));
-        const bool more = j + 1 < n_kv;
-        if (more) {
-          if (!(ok = mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status))) break;
+      // The key-tile loop, compiled once for two query tiles and once for one: a run-time
+      // branch on the tile count inside this one-lane issue loop costs about 1% of the kernel.
+      auto mma_loop = [&](auto two_tiles) {
+        constexpr bool TWO = decltype(two_tiles)::value;
+        bool ok = mbar_wait(q_full, 0, abort, p.status);
+        if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), abort, p.status);
+        if (ok) {
           tc_fence_after();
-          issue_s(0, slot_of(itk));
+          issue_s(0, slot_of(0));
           mma_commit(s_full(0));
-        }
-        if (two) {
-          if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
-          tc_fence_after();
-          issue_pv(1, slot_of(itv), j > 0);
-          mma_commit(o_bar(1));
-        }
-        mma_commit(empty_bar(slot_of(itv)));
-        if (more) {
-          if (two) {
-            issue_s(1, slot_of(itk));
+          if constexpr (TWO) {
+            issue_s(1, slot_of(0));
             mma_commit(s_full(1));
           }
-          mma_commit(empty_bar(slot_of(itk)));
+          mma_commit(empty_bar(slot_of(0)));
         }
-      }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int itv = 2 * j + 1, itk = 2 * j + 2;
+          if (!(ok = mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status))) break;
+          if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_pv(0, slot_of(itv), j > 0);
+          mma_commit(o_bar(0));
+          const bool more = j + 1 < n_kv;
+          if (more) {
+            if (!(ok = mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status))) break;
+            tc_fence_after();
+            issue_s(0, slot_of(itk));
+            mma_commit(s_full(0));
+          }
+          if constexpr (TWO) {
+            if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+            tc_fence_after();
+            issue_pv(1, slot_of(itv), j > 0);
+            mma_commit(o_bar(1));
+          }
+          mma_commit(empty_bar(slot_of(itv)));
+          if (more) {
+            if constexpr (TWO) {
+              issue_s(1, slot_of(itk));
+              mma_commit(s_full(1));
+            }
+            mma_commit(empty_bar(slot_of(itk)));
+          }
+        }
+      };
+      if (two)
+        mma_loop(std::true_type{});
+      else
+        mma_loop(std::false_type{});
       // drain: every MMA issued above has finished before TMEM is released
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, abort, p.status);
