@@ -43,6 +43,7 @@
 //   warps 14-15 idle
 // Tensor memory (512 columns): dV | dK | S^T (later P^T) | dP^T (then dQ_i).
 #include <algorithm>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "sm103.cuh"
@@ -249,19 +250,21 @@ __global__ void __launch_bounds__(512, 1)
       ss_kmajor(C::COL_DP, sV, sDO(0));
       mma_commit(dp_full, leader);
     }
-    for (int t = 0; ok && t < ntiles; ++t) {
+    // one query tile; MORE: another tile follows (the last iteration is peeled so that the
+    // test is not a run-time branch of the issue loop)
+    auto step = [&](int t, auto more_tiles) -> bool {
+      constexpr bool MORE = decltype(more_tiles)::value;
       const int s = t & 1;
-      const bool more = t + 1 < ntiles;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, abort, p.status)))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, abort, p.status))) return false;
       tc_fence_after();
       ts_acc(C::COL_DV, C::COL_S, sDO(s), t > 0);  // dV += P^T dO_t
-      if (more) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status)))) break;
+      if constexpr (MORE) {
+        if (!__all_sync(0xffffffffu, mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status))) return false;
         tc_fence_after();
         ss_kmajor(C::COL_S, sK, sQ(s ^ 1));  // S^T of the next tile (P^T_t already consumed)
         mma_commit(s_full, leader);
       }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_ready, t & 1, abort, p.status)))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(ds_ready, t & 1, abort, p.status))) return false;
       tc_fence_after();
       // dQ first, so its read-out overlaps the dK MMA
       if constexpr (C::DQ_T) {
@@ -285,13 +288,16 @@ __global__ void __launch_bounds__(512, 1)
         mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                sdesc_sw128(sQ(s) + kk * 2048, 16384, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u, leader);
       mma_commit(st_empty(s), leader);
-      if (more) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_empty, t & 1, abort, p.status)))) break;
+      if constexpr (MORE) {
+        if (!__all_sync(0xffffffffu, mbar_wait(dq_empty, t & 1, abort, p.status))) return false;
         tc_fence_after();
         ss_kmajor(C::COL_DP, sV, sDO(s ^ 1));
         mma_commit(dp_full, leader);
       }
-    }
+      return true;
+    };
+    for (int t = 0; ok && t + 1 < ntiles; ++t) ok = step(t, std::true_type{});
+    if (ok && ntiles > 0) ok = step(ntiles - 1, std::false_type{});
     mma_commit(mma_done, leader);
     __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
   } else if (warp < 8) {

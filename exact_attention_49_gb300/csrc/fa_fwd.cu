@@ -199,35 +199,40 @@ __global__ void __launch_bounds__(320, 1)
           }
           mma_commit(empty_bar(slot_of(0)));
         }
-        for (int j = 0; ok && j < n_kv; ++j) {
+        // one key tile; MORE: another tile follows (the last iteration is peeled so that
+        // neither test is a run-time branch of the issue loop)
+        auto step = [&](int j, auto more_tiles) -> bool {
+          constexpr bool MORE = decltype(more_tiles)::value;
           const int itv = 2 * j + 1, itk = 2 * j + 2;
-          if (!(ok = mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status))) break;
-          if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
+          if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status)) return false;
+          if (!mbar_wait(p_full(0), j & 1, abort, p.status)) return false;
           tc_fence_after();
           issue_pv(0, slot_of(itv), j > 0);
           mma_commit(o_bar(0));
-          const bool more = j + 1 < n_kv;
-          if (more) {
-            if (!(ok = mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status))) break;
+          if constexpr (MORE) {
+            if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status)) return false;
             tc_fence_after();
             issue_s(0, slot_of(itk));
             mma_commit(s_full(0));
           }
           if constexpr (TWO) {
-            if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+            if (!mbar_wait(p_full(1), j & 1, abort, p.status)) return false;
             tc_fence_after();
             issue_pv(1, slot_of(itv), j > 0);
             mma_commit(o_bar(1));
           }
           mma_commit(empty_bar(slot_of(itv)));
-          if (more) {
+          if constexpr (MORE) {
             if constexpr (TWO) {
               issue_s(1, slot_of(itk));
               mma_commit(s_full(1));
             }
             mma_commit(empty_bar(slot_of(itk)));
           }
-        }
+          return true;
+        };
+        for (int j = 0; ok && j + 1 < n_kv; ++j) ok = step(j, std::true_type{});
+        if (ok) step(n_kv - 1, std::false_type{});
       };
       if (two)
         mma_loop(std::true_type{});
