@@ -123,3 +123,49 @@ def test_bwd_validation(L):
     assert bwd(det=2) == fa.FA_ERR_INVALID_ARG
     assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert bwd(N=0, q=None, ws=None) == fa.FA_OK
+
+
+def test_qk_and_splitkv_validation(L):
+    """fa_fwd_qk / fa_bwd_qk / fa_fwd_splitkv reject bad arguments before any launch."""
+    from exact_attention_49_gb300 import binding as fa
+
+    def fwd_qk(q=GOOD, k=GOOD, B=1, H=2, Hkv=1, Nq=64, Nk=300, d=64, causal=1, scale=0.125):
+        return L.fa_fwd_qk(q, k, GOOD, GOOD, GOOD, B, H, Hkv, Nq, Nk, d, causal, scale, None)
+
+    assert fwd_qk(q=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd_qk(Nk=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd_qk(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_qk(k=BAD) == fa.FA_ERR_MISALIGNED
+    assert fwd_qk(causal=3) == fa.FA_ERR_INVALID_ARG
+    assert fwd_qk(Nq=0, q=None, k=None) == fa.FA_OK  # no query: nothing to do
+
+    def bwd_qk(q=GOOD, Nq=64, Nk=300, d=64, ws=GOOD, wsb=1 << 30, det=0):
+        return L.fa_bwd_qk(q, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, 1, 2, 1, Nq, Nk, d, 1, 0.125, det,
+                           ws, wsb, None)
+
+    assert bwd_qk(q=None) == fa.FA_ERR_INVALID_ARG
+    assert bwd_qk(Nk=-3) == fa.FA_ERR_INVALID_ARG
+    assert bwd_qk(ws=None) == fa.FA_ERR_WORKSPACE
+    assert bwd_qk(det=5) == fa.FA_ERR_INVALID_ARG
+    # the workspace depends on Nq only (rows padded to 128), not on Nk
+    w1 = fa.fa_bwd_qk_workspace_bytes(1, 2, 1, 64, 300, 64, 0)
+    assert w1 == fa.fa_bwd_qk_workspace_bytes(1, 2, 1, 100, 5000, 64, 0) == fa.fa_bwd_workspace_bytes(1, 2, 1, 128, 64, 0)
+    assert fa.fa_bwd_qk_workspace_bytes(1, 2, 1, 64, -1, 64, 0) == 0
+
+    def dec(splits=4, ws=GOOD, wsb=1 << 30, Nq=1, Nk=4096, d=128):
+        return L.fa_fwd_splitkv(GOOD, GOOD, GOOD, GOOD, GOOD, 2, 8, 2, Nq, Nk, d, 1, 0.125, splits, ws, wsb, None)
+
+    assert dec(splits=-1) == fa.FA_ERR_INVALID_ARG
+    assert dec(splits=5000) == fa.FA_ERR_INVALID_ARG
+    assert dec(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert dec(ws=None) == fa.FA_ERR_WORKSPACE
+    assert dec(wsb=16) == fa.FA_ERR_WORKSPACE
+    assert dec(ws=P((1 << 20) + 16)) == fa.FA_ERR_MISALIGNED
+    # one split needs no workspace; several need room for their fp32 partials and LSEs
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 4096, 128, 1) == 0
+    rows = 2 * 8 * 1
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 4096, 128, 4) >= 4 * rows * 128 * 4 + 4 * rows * 4
+    # more splits than key tiles are clamped to the key tiles
+    assert (fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 256, 128, 64)
+            == fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 256, 128, 2))
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 4096, 128, 0) > 0
