@@ -5,27 +5,30 @@
 // recomputation paragraph).  Three kernels:
 //
 //   preprocess   per query row: D = sum_c dO_c O_c (fp32) and LSE in log2 units
-//                (two fp32 arrays); zero the fp32 dQ accumulator (and, in the
+//                (two fp32 arrays, rows padded per head to a multiple of 128 with
+//                LSE = +inf, D = 0); zero the fp32 dQ accumulator (and, in the
 //                deterministic mode, the ordering counters).
 //   main         one CTA per (b, K/V head g, 128-key tile j).  It keeps K_j, V_j in
 //                shared memory and dK, dV accumulators in tensor memory for the
 //                whole run, and walks every (query head of the group, 128-row
-//                query tile i) pair that can see the tile (causal: i >= j).  Per
+//                query tile i) pair that can see the tile (causal: query row q sits
+//                at position q + Nk - Nq, so i starts where a row reaches key 128 j).  Per
 //                pair, five tcgen05 GEMMs (M = 128):
 //                  S^T  = K_j Q_i^T        (TMEM, fp32)
 //                  dP^T = V_j dO_i^T       (TMEM, fp32)
 //                  P^T  = exp2(S^T * scale*log2e - lse2_i)     (bf16, over S^T in TMEM)
 //                  dS^T = P^T * (dP^T - D_i) * scale           (bf16, in shared memory)
 //                  dV  += P^T dO_i  (A from TMEM),  dK += dS^T Q_i  (A from shared memory)
-//                  dQ_i = dS K_j                               (TMEM, then fp32
-//                                                               reductions into the
-//                                                               dQ accumulator)
+//                  dQ_i = dS K_j  (d = 128: as dQ_i^T = K_j^T dS^T, so that a TMEM lane
+//                                  is a head-dim column; TMEM, then fp32 reductions
+//                                  into the dQ accumulator)
 //                Grouped heads (GQA) share K_j/V_j, so dK/dV are summed over the
 //                group inside the CTA, in a fixed order, without atomics.
 //   postprocess  dQ accumulator (already scaled) -> bf16.
 //
 // The dQ accumulation over key tiles is the only cross-CTA sum.  Default: fp32
-// vector reductions (red.global.add.v4.f32) in whatever order CTAs reach them.
+// reductions (coalesced red.global.add.f32 for d = 128, red.global.add.v4.f32 for
+// d = 64) in whatever order CTAs reach them.
 // Deterministic mode (FA4's deterministic backward, wiki 未解決の問い): the CTA
 // of key tile j waits (bounded) until the key tiles ranked before it have added
 // their part of query tile i — tiles 0..j-1 in general, the tiles above j when
@@ -38,7 +41,8 @@
 //   warps 0-3   compute, query columns 0-63 of each tile (thread = key row = TMEM lane)
 //   warps 4-7   compute, query columns 64-127
 //   warps 8-11  dQ read-out and reduction; at the end the dK/dV epilogue
-//   warp 12     MMA issuer (one thread) and TMEM allocator
+//   warp 12     MMA issuer (the warp runs the loop converged, lane 0 issues) and
+//               TMEM allocator
 //   warp 13     TMA producer (one thread)
 //   warps 14-15 idle
 // Tensor memory (512 columns): dV | dK | S^T (later P^T) | dP^T (then dQ_i).

@@ -23,6 +23,14 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; P (bf16) overwrites the first
 // half of its S block and feeds the PV MMA straight from TMEM.
 // Shared memory: Q0, Q1 and a ring of K/V tiles (K_j and V_j take turns).
+//
+// Variants of the same kernel:
+//   Nq != Nk     the causal mask places query row i at position i + (Nk - Nq);
+//   one tile     a block with at most 128 rows runs query tile 0 only;
+//   split-KV     (decoding) several CTAs share a block's key tiles, each writing an
+//                fp32 partial O and its LSE, merged by fwd_combine_kernel; the query
+//                heads of a K/V group are packed as the rows of one block, each row
+//                keeping its own causal position (pos_mod).
 #include <algorithm>
 #include <type_traits>
 
