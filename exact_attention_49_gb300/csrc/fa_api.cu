@@ -107,7 +107,7 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 static int check_shape(int B, int H, int Hkv, int N, int d) {
   if (B < 0 || H < 1 || Hkv < 1 || N < 0) return FA_ERR_INVALID_ARG;
   if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H > (1LL << 30) || N > (1 << 30)) return FA_ERR_INVALID_ARG;
   if ((long long)B * H * ((N + 255) / 256) > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   return FA_OK;
@@ -228,7 +228,8 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.pos_mod = 0;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
-  const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;
+  // the exponential-split ablation is built for d = 64 and 128 only
+  const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
@@ -317,7 +318,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   p.lse_part = S > 1 ? reinterpret_cast<float*>(ws + ((size_t)S * all_rows * d * 4 + 255) / 256 * 256) : nullptr;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
-  const int poly = options().poly_exp < 0 ? kDefaultPolyCols : options().poly_exp;
+  // the exponential-split ablation is built for d = 64 and 128 only
+  const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, s);
   if (e == cudaSuccess && S > 1) e = launch_fwd_combine(d, p.o_part, p.lse_part, o, lse, S, (long long)all_rows, s);
@@ -347,7 +349,7 @@ static BwdWorkspace bwd_ws_layout(int B, int H, int Nq, int d, int deterministic
 }
 
 size_t fa_bwd_qk_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int deterministic) {
-  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d)) return 0;
+  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d) || d == 256) return 0;
   if (deterministic != 0 && deterministic != 1) return 0;
   return bwd_ws_layout(B, H, Nq, d, deterministic).total;
 }
@@ -362,6 +364,7 @@ static int check_bwd_common(int B, int H, int Hkv, int Nq, int d, int determinis
                             size_t ws_bytes) {
   int st = check_shape(B, H, Hkv, Nq, d);
   if (st) return st;
+  if (d == 256) return fail_detail(FA_ERR_UNSUPPORTED, "the backward supports d = 64 and 128");
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
   if (B == 0 || Nq == 0) return 1;
   if (!ws) return FA_ERR_WORKSPACE;

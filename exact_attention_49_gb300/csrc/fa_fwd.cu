@@ -1,7 +1,8 @@
 // fa_fwd.cu -- exact attention forward for sm_103a.
 //
-// One CTA owns two query tiles of 128 rows (256 consecutive rows of one head)
-// and walks the key/value tiles of 128 rows of that head:
+// One CTA owns two query tiles of 128 rows (256 consecutive rows of one head;
+// one tile of 128 rows at d = 256) and walks the key/value tiles of 128 rows of
+// that head:
 //
 //   tiling      -- "FlashAttention" wiki note, 定義 item (1); the explainer's
 //                  tiling paragraph (blocks loaded from HBM into on-chip memory,
@@ -45,13 +46,17 @@ struct FwdCfg {
   static constexpr int BN = 128;                    // keys per K/V tile
   static constexpr int TILE = 128 * D * 2;          // bytes of one 128 x D bf16 tile
   static constexpr int CHUNKS = D / 64;             // 128-byte swizzle atoms across D
-  static constexpr int STAGES = (D == 128) ? 4 : 8; // K/V ring slots
-  static constexpr int SMEM_Q = 2 * TILE;
+  // query tiles per CTA: two (S0 | S1 | O0 | O1 in TMEM), or one at d = 256 (S0 | O0 already
+  // take 384 of the 512 columns)
+  static constexpr int NT = (D == 256) ? 1 : 2;
+  static constexpr int BLOCK = 128 * NT;            // query rows per CTA
+  static constexpr int STAGES = (D == 256) ? 2 : (D == 128) ? 4 : 8;  // K/V ring slots
+  static constexpr int SMEM_Q = NT * TILE;
   static constexpr int SMEM_RING = STAGES * TILE;
   static constexpr int NBAR = 2 * STAGES + 8;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
   static constexpr int THREADS = 320;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = (NT == 2) ? 256 : 128, COL_O1 = 256 + D;
 };
 
 // POLY: how many of every 16 column pairs take the FMA-pipe polynomial exp2 instead of
@@ -82,7 +87,7 @@ __global__ void __launch_bounds__(320, 1)
 
   // ---- work unit: (b, h, block of 256 query rows); causal: heaviest blocks first
   const int N = p.Nq;  // query rows; keys: p.Nk
-  const int ncb = (N + 255) / 256;
+  const int ncb = (N + C::BLOCK - 1) / C::BLOCK;
   const int BH = p.B * p.H;
   const int sp = blockIdx.x % p.splits;  // key-range split (split-KV); 0 when splits = 1
   const int t = blockIdx.x / p.splits;
@@ -90,11 +95,11 @@ __global__ void __launch_bounds__(320, 1)
   const int bh = t % BH;
   const int b = bh / p.H, h = bh % p.H;
   const int g = h / (p.H / p.Hkv);
-  const int q0 = cb * 256;
+  const int q0 = cb * C::BLOCK;
   const int n_kv_all = (p.Nk + 127) / 128;
   // causal: the block's last row (position row + qoff) bounds the key tiles it needs; a block
   // whose rows see no key at all still runs one fully masked tile (O = 0, LSE = -inf)
-  const int last_row = min(q0 + 255, N - 1);
+  const int last_row = min(q0 + C::BLOCK - 1, N - 1);
   const int k_last = (p.pos_mod ? min(last_row, p.pos_mod - 1) : last_row) + p.qoff;
   const int n_vis = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
   // this CTA's key tiles [j0, j0 + n_kv); a split whose range holds no visible key still runs
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(320, 1)
   const int j0 = sp * p.split_tiles;
   const int n_kv = max(1, min(n_vis, j0 + p.split_tiles) - j0);
   // a block with at most 128 rows (a ragged last block; decoding) runs query tile 0 only
-  const bool two = N - q0 > 128;
+  const bool two = C::NT == 2 && N - q0 > 128;
   const int kv_z = b * p.Hkv + g;
 
   if (warp == 0 && lane == 0) {
@@ -137,8 +142,8 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
-      for (int qt = 0; qt < 2; ++qt)
+      mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
+      for (int qt = 0; qt < C::NT; ++qt)
         for (int ch = 0; ch < C::CHUNKS; ++ch)
           tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, q0 + qt * 128, bh);
       int issued = 0;
@@ -415,7 +420,7 @@ static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, c
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)((p.Nq + 255) / 256) * p.B * p.H * p.splits;
+  const long long blocks = (long long)((p.Nq + C::BLOCK - 1) / C::BLOCK) * p.B * p.H * p.splits;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   fwd_kernel<D, POLY><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
@@ -437,6 +442,10 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int poly_cols, cudaStream_t stream) {
   if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, poly_cols, stream);
+  if (d == 256) {  // MUFU exponentials only at d = 256
+    if (poly_cols != 0) return cudaErrorInvalidValue;
+    return launch_fwd_dp<256, 0>(tq, tk, tv, p, stream);
+  }
   return launch_fwd_d<128>(tq, tk, tv, p, poly_cols, stream);
 }
 
@@ -447,7 +456,7 @@ template <int D>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ lse_part, uint16_t* __restrict__ o,
                                                           float* __restrict__ lse, int S, long long rows) {
-  constexpr int PER = D / 32;  // fp32 elements per lane (4 or 2)
+  constexpr int PER = D / 32;  // fp32 elements per lane (2, 4 or 8)
   const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   for (long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); row < rows; row += nwarps) {
@@ -486,6 +495,8 @@ cudaError_t launch_fwd_combine(int d, const float* o_part, const float* lse_part
   const int grid = (int)std::min<long long>(std::max<long long>(want, 1), 4096);
   if (d == 64)
     fwd_combine_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o), lse, splits, rows);
+  else if (d == 256)
+    fwd_combine_kernel<256><<<grid, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o), lse, splits, rows);
   else
     fwd_combine_kernel<128><<<grid, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o), lse, splits, rows);
   return cudaGetLastError();

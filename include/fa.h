@@ -40,8 +40,10 @@
  * that gives up (bounded at about 2 s) records FA_ERR_DEVICE_TIMEOUT in a
  * device status word, read and cleared by fa_last_device_status.
  *
- * Supported: d in {64, 128}; H % Hkv == 0; 16-byte aligned bf16 pointers,
- * 4-byte aligned lse; any N >= 0; scale finite and > 0; an sm_103 device.
+ * Supported: d in {64, 128, 256} for the forward entry points and {64, 128}
+ * for the backward (at d = 256 the backward's dK, dV accumulators alone would
+ * fill tensor memory); H % Hkv == 0; 16-byte aligned bf16 pointers, 4-byte
+ * aligned lse; any N >= 0; scale finite and > 0; an sm_103 device.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -55,7 +57,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = -1,     /* null pointer, bad size, H % Hkv != 0, bad scale */
-  FA_ERR_UNSUPPORTED = -2,     /* d not in {64,128}, N not supported, not an sm_103 device */
+  FA_ERR_UNSUPPORTED = -2,     /* d not supported, not an sm_103 device */
   FA_ERR_MISALIGNED = -3,      /* a pointer is not aligned as required */
   FA_ERR_WORKSPACE = -4,       /* workspace missing or smaller than fa_bwd_workspace_bytes */
   FA_ERR_CUDA = -5,            /* a CUDA runtime/driver call or a launch failed */

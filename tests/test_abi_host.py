@@ -78,7 +78,7 @@ def test_fwd_validation(L):
     assert fwd(L, lse=None) == fa.FA_ERR_INVALID_ARG
     assert fwd(L, H=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
     assert fwd(L, d=96) == fa.FA_ERR_UNSUPPORTED
-    assert fwd(L, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(L, d=192) == fa.FA_ERR_UNSUPPORTED  # d = 256 is a forward-only size
     assert fwd(L, q=BAD) == fa.FA_ERR_MISALIGNED
     assert fwd(L, o=BAD) == fa.FA_ERR_MISALIGNED
     assert fwd(L, lse=P((1 << 20) + 2)) == fa.FA_ERR_MISALIGNED
@@ -101,6 +101,7 @@ def test_workspace_size(L):
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, d, 1) > ws
     assert fa.fa_bwd_workspace_bytes(B, 3, 2, N, d, 0) == 0
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 96, 0) == 0
+    assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 256, 0) == 0
     # rows are padded per head to a multiple of 128
     assert fa.fa_bwd_workspace_bytes(B, H, 2, 200, d, 0) == fa.fa_bwd_workspace_bytes(B, H, 2, 256, d, 0)
     assert fa.fa_bwd_workspace_bytes(B, H, 2, 1, d, 1) == fa.fa_bwd_workspace_bytes(B, H, 2, 128, d, 1)
@@ -114,6 +115,7 @@ def test_bwd_validation(L):
     assert bwd(q=None) == fa.FA_ERR_INVALID_ARG
     assert bwd(H=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
     assert bwd(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(d=256) == fa.FA_ERR_UNSUPPORTED  # the backward supports d = 64 and 128
     # any N is accepted; a ragged N needs the workspace of N rounded up to 128 rows per head
     assert bwd(N=200, wsb=fa.fa_bwd_workspace_bytes(1, 2, 1, 200, 64, 0) - 256) == fa.FA_ERR_WORKSPACE
     assert bwd(ws=None) == fa.FA_ERR_WORKSPACE
