@@ -15,6 +15,8 @@ Contents
 ``online.py``     a separate CPU online-softmax forward (tile by tile, running
                   max and sum, rescale when the max grows), used to pin the
                   exactness claim of the tiled method.
+``fp8.py``        attention on FP8 (e4m3) operands: block or per-tensor scaling and
+                  the incoherent-processing rotation, for the FP8 variant.
 
 Every function cites the passage of the pages it follows.  Pins (tests that
 check the oracle against something other than itself) live in
