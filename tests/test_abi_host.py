@@ -171,3 +171,42 @@ def test_qk_and_splitkv_validation(L):
     assert (fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 256, 128, 64)
             == fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 256, 128, 2))
     assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 2, 1, 4096, 128, 0) > 0
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/fa.h is usable from C99 (no C++ in the interface): a translation unit that
+    calls every entry point compiles with gcc -std=c99 -Wall -Wextra -Werror."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_fa.c"
+    src.write_text(r'''
+#include <stddef.h>
+#include "fa.h"
+int use_fa(void* q, void* k, void* v, void* o, float* lse, void* ws, size_t wsb) {
+  int st = fa_fwd(q, k, v, o, lse, 1, 2, 1, 128, 64, 1, 0.125f, NULL);
+  st |= fa_fwd_qk(q, k, v, o, lse, 1, 2, 1, 1, 128, 64, 1, 0.125f, NULL);
+  st |= fa_fwd_splitkv(q, k, v, o, lse, 1, 2, 1, 1, 128, 64, 1, 0.125f, 0, ws,
+                       fa_fwd_splitkv_workspace_bytes(1, 2, 1, 1, 128, 64, 0), NULL);
+  st |= fa_bwd(q, k, v, o, o, lse, q, k, v, 1, 2, 1, 128, 64, 1, 0.125f, 0, ws,
+               fa_bwd_workspace_bytes(1, 2, 1, 128, 64, 0), NULL);
+  st |= fa_bwd_qk(q, k, v, o, o, lse, q, k, v, 1, 2, 1, 64, 128, 64, 1, 0.125f, 1, ws,
+                  fa_bwd_qk_workspace_bytes(1, 2, 1, 64, 128, 64, 1), NULL);
+  st |= fa_bwd_preprocess(o, o, lse, 1, 2, 1, 128, 64, 0, ws, wsb, NULL);
+  st |= fa_bwd_main(q, k, v, o, lse, k, v, 1, 2, 1, 128, 64, 1, 0.125f, 0, ws, wsb, NULL);
+  st |= fa_bwd_postprocess(q, 1, 2, 1, 128, 64, 0, ws, wsb, NULL);
+  st |= fa_bwd_noalloc(q, k, v, o, o, lse, q, k, v, 1, 2, 1, 128, 64, 1, 0.125f, 0, NULL);
+  double val = 0.0;
+  st |= fa_set_option("rescale_threshold", 8.0) | fa_get_option("rescale_threshold", &val);
+  (void)fa_status_string(st);
+  (void)fa_last_error_detail();
+  st |= fa_last_device_status(NULL) | fa_version();
+  return st + (val > 0.0 ? 0 : 1) + (int)(FA_NOALLOC_SCRATCH_BYTES > 0u);
+}
+''')
+    out = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-c", str(src),
+                          "-I", os.path.join(ROOT, "include"), "-o", str(tmp_path / "use_fa.o")],
+                         capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
