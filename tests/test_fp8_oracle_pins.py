@@ -1,10 +1,11 @@
 """Pins of the FP8 attention reference (oracle/fp8.py) against things other than
 itself: the e4m3 bit layout enumerated exhaustively, torch's own e4m3 cast, the
 orthogonality of the rotation, the exactness of attention under the rotation
-without rounding, the e4m3 relative-error bound, and an error study on inputs
-with outlier features (block quantisation with incoherent processing against
-per-tensor FP8, the comparison the pages make; the pages' 2.6x gain is not
-reproduced under these readings, see the study's docstring)."""
+without rounding, the e4m3 relative-error bound, hand-derived values of the
+block and per-tensor quantisers and of the P quantisation, and an error study
+(block quantisation with incoherent processing against per-tensor FP8, the
+comparison the pages make) on inputs with outlier feature columns, where the
+pages' 2.6x gain is reproduced."""
 import numpy as np
 import pytest
 import torch
@@ -85,14 +86,12 @@ def _outlier_inputs(seed, B=1, H=2, N=512, d=128):
 
 
 def test_fp8_error_study_on_outlier_inputs():
-    """The pages report 2.6x lower error for block quantisation with incoherent processing
-    than for baseline FP8.  Under the readings of oracle/fp8.py (e4m3 with amax scaling per
-    128-row block or per tensor, a random-sign Hadamard rotation, P in e4m3) the measured
-    gain on this recipe is small: e4m3 keeps about 2^-4 relative error over 17 binades, so
-    outliers of this size never push typical values out of its normal range, and the P and
-    V roundings, equal in every mode, set the error floor.  The test pins what holds: every
-    mode stays within the e4m3 error scale, the block modes are not worse than per-tensor,
-    and the rotation does not change which mode is best by more than a few percent."""
+    """Scattered element outliers (0.1% of entries, scale 10) are not the case incoherent
+    processing targets: e4m3 keeps about 2^-4 relative error over 17 binades, so outliers of
+    this size never push typical values out of its normal range, and the P and V roundings,
+    equal in every mode, set the error floor; the gain is small here.  The test pins what
+    holds: every mode stays within the e4m3 error scale and the block modes are not worse
+    than per-tensor.  (Outlier feature columns, below, reproduce the pages' gain.)"""
     for seed in range(3):
         q, k, v = _outlier_inputs(seed)
         scale = 128 ** -0.5
@@ -105,3 +104,104 @@ def test_fp8_error_study_on_outlier_inputs():
         assert max(rmse.values()) < 0.05, rmse
         assert rmse["block"] <= rmse["tensor"] * 1.1, rmse
         assert rmse["block_incoherent"] <= rmse["tensor"] * 1.1, rmse
+
+
+# ---------------------------------------------------------------- hand-derived quantiser values
+# e4m3 keeps 3 mantissa bits in every binade of its normal range [2^-6, 448], so a common
+# power-of-ten rescaling changes nothing there; block and per-tensor scales differ only where
+# one of them pushes a block into the subnormal range (quantum 2^-9).  Each expected value is
+# derived in the comment beside it.
+
+def test_quantize_blocks_two_blocks_with_different_scales():
+    x = np.array([[4.0], [1.0], [1e-4], [2e-4]])[None, None]        # [1, 1, N=4, d=1], block = 2
+    got = fp8.quantize_blocks(x, block=2)[0, 0, :, 0]
+    # block 0: amax 4, s = 4/448 = 1/112: 4 -> 448 and 1 -> 112 = 1.75 * 2^6 are exact
+    # block 1: amax 2e-4, s = 2e-4/448: 2e-4 -> 448 and 1e-4 -> 224 = 1.75 * 2^7 are exact
+    np.testing.assert_allclose(got, [4.0, 1.0, 1e-4, 2e-4], rtol=1e-15, atol=0)
+
+
+def test_quantize_tensor_uses_one_scale_for_the_whole_tensor():
+    x = np.array([[4.0], [1.0], [1e-4], [2e-4]])[None, None]
+    got = fp8.quantize_tensor(x)[0, 0, :, 0]
+    # one scale s = 4/448 = 1/112 for all four values:
+    #   1e-4 * 112 = 0.0112 < 2^-6 is subnormal: 0.0112 * 2^9 = 5.73 -> 6, value 6 * 2^-9 / 112
+    #   2e-4 * 112 = 0.0224 in [2^-6, 2^-5), spacing 2^-9: 0.0224 * 2^9 = 11.47 -> 11
+    expect = [4.0, 1.0, 6 * 2.0 ** -9 / 112, 11 * 2.0 ** -9 / 112]
+    np.testing.assert_allclose(got, expect, rtol=1e-15, atol=0)
+
+
+def test_quantize_blocks_never_spans_two_heads():
+    # two heads of two rows each, block = 128: each head is one block of its own, so the small
+    # head keeps its own scale (exact values) instead of the large head's (subnormal values)
+    x = np.array([[[4.0], [1.0]], [[1e-4], [2e-4]]])[None]           # [1, H=2, N=2, d=1]
+    got = fp8.quantize_blocks(x, block=128)[0, :, :, 0]
+    np.testing.assert_allclose(got, [[4.0, 1.0], [1e-4, 2e-4]], rtol=1e-15, atol=0)
+
+
+def test_quantize_blocks_rounds_inside_a_binade_with_ties_to_even():
+    x = np.array([[1.0], [3.0], [4.0], [0.01]])[None, None]          # one block, s = 1/112
+    got = fp8.quantize_blocks(x, block=128)[0, 0, :, 0]
+    # 3 -> 336 in [256, 512), spacing 32: 336 / 32 = 10.5 -> 10 (even) -> 320 / 112
+    # 0.01 -> 1.12 in [1, 2), spacing 1/8: 8.96 -> 9 -> 1.125 / 112
+    np.testing.assert_allclose(got, [1.0, 320 / 112, 4.0, 1.125 / 112], rtol=1e-15, atol=0)
+
+
+def test_p_quantisation_and_normalisation_closed_form():
+    # one query, three keys (scale 1, no rotation): scores q.k = (0, 0, 1), all inputs exact
+    # in e4m3 under their block scales (Q, K: amax 1; V: amax 4, v/s = 112, 224, 448)
+    q = np.array([[[[1.0, 0.0]]]])
+    k = np.array([[[[0.0, 1.0], [0.0, 1.0], [1.0, 0.0]]]])
+    v = np.array([[[[1.0, 0.0], [2.0, 0.0], [4.0, 0.0]]]])
+    o, lse = fp8.fp8_attention(q, k, v, False, 1.0, mode="block")
+    # P = (1, 1, e) / (2 + e); 448 P = (94.95, 94.95, 258.1):
+    #   94.95 in [64, 128), spacing 8: 11.87 -> 12 -> 96;  258.1 in [256, 512), spacing 32: 8.07 -> 8 -> 256
+    # O = (96 * 1 + 96 * 2 + 256 * 4) / (96 + 96 + 256): normalised by the quantised weights
+    assert o[0, 0, 0, 0] == pytest.approx(1312 / 448, rel=1e-15)
+    assert o[0, 0, 0, 1] == 0.0
+    # (here the quantised weights happen to sum to 448, so the next test checks the normaliser)
+    assert lse[0, 0, 0] == pytest.approx(np.log(2 + np.e), rel=1e-15)   # LSE of the unquantised softmax
+
+
+def test_p_quantisation_normalises_by_the_quantised_sum():
+    # scores (0, 0, ln 3) are not exact, so build them from scale: q.k = (0, 0, 1), scale = ln 3
+    q = np.array([[[[1.0, 0.0]]]])
+    k = np.array([[[[0.0, 1.0], [0.0, 1.0], [1.0, 0.0]]]])
+    v = np.array([[[[1.0, 0.0], [2.0, 0.0], [4.0, 0.0]]]])
+    o, lse = fp8.fp8_attention(q, k, v, False, float(np.log(3.0)), mode="block")
+    # P = (1, 1, 3) / 5 = (0.2, 0.2, 0.6); 448 P = (89.6, 89.6, 268.8):
+    #   89.6 in [64, 128), spacing 8: 11.2 -> 11 -> 88;  268.8 in [256, 512), spacing 32: 8.4 -> 8 -> 256
+    # sum of the quantised weights 88 + 88 + 256 = 432 (not 448):
+    #   O = (88 + 176 + 1024) / 432;  dividing by the unquantised sum would give 1288 / 448
+    assert o[0, 0, 0, 0] == pytest.approx(1288 / 432, rel=1e-15)
+    assert lse[0, 0, 0] == pytest.approx(np.log(5.0), rel=1e-14)
+
+
+def _channel_outlier_inputs(seed, mag, N=512, d=128, H=2, ncols=4):
+    # N(0,1) entries; a few head-dim columns of Q and K scaled by `mag` (the outlier features
+    # that incoherent processing spreads over all dimensions)
+    rng = np.random.default_rng(seed)
+    q, k, v = (rng.standard_normal((1, H, N, d)) for _ in range(3))
+    cols = rng.choice(d, ncols, replace=False)
+    q[..., cols] *= mag
+    k[..., cols] *= mag
+    return q, k, v
+
+
+@pytest.mark.parametrize("mag", [10.0, 50.0, 100.0])
+def test_fp8_incoherent_processing_gain_on_outlier_channels(mag):
+    """The wiki's FA3 item 3 reports 2.6x lower error for block quantisation with incoherent
+    processing than for baseline (per-tensor) FP8.  With outlier feature columns (4 of 128
+    head-dim columns of Q and K scaled by 10-100) the rotation spreads each outlier over all
+    columns before rounding; the O error drops by 2.1-4.5x here (two seeds per magnitude), so
+    the claim holds in this regime: the pin is a gain of at least 2x on both seeds, and at
+    least 1.5x on the LSE error."""
+    for seed in range(2):
+        q, k, v = _channel_outlier_inputs(seed, mag)
+        scale = 128 ** -0.5
+        o_ref, lse_ref = ref.attn_fwd(q, k, v, True, scale)
+        err = {}
+        for mode in ("tensor", "block_incoherent"):
+            o, lse = fp8.fp8_attention(q, k, v, True, scale, mode=mode, seed=seed)
+            err[mode] = (float(np.sqrt(np.mean((o - o_ref) ** 2))), float(np.mean(np.abs(lse - lse_ref))))
+        assert err["tensor"][0] >= 2.0 * err["block_incoherent"][0], err
+        assert err["tensor"][1] >= 1.5 * err["block_incoherent"][1], err
