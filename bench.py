@@ -191,6 +191,8 @@ def cpu_oracle_sample(w, q, k, v, do, budget_s=12.0, max_heads=8):
 
 def run_reference(args, w):
     ws, rank, _ = dist_setup()
+    if args.gpus != ws:
+        raise SystemExit("bench.py --gpus %d but WORLD_SIZE=%d" % (args.gpus, ws))
     if rank != 0:
         return 0
     import torch
@@ -248,6 +250,10 @@ def run_ours(args, w):
     from exact_attention_49_gb300.inputs import workload_inputs
 
     ws, rank, local = dist_setup()
+    if args.gpus != ws:
+        raise SystemExit("bench.py --gpus %d but WORLD_SIZE=%d: launch one process per GPU with "
+                         "python -m torch.distributed.run --nproc-per-node %d bench.py --gpus %d"
+                         % (args.gpus, ws, args.gpus, args.gpus))
     torch.cuda.set_device(local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -493,7 +499,9 @@ def run_decode(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    # 200 steps of the default workload keep the timed region near 0.7 s, long enough for the
+    # clock sampler (every 20 ms) to see it under load
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="C3")

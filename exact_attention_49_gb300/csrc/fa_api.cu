@@ -17,6 +17,9 @@ namespace fa {
 
 // The library's device status word (one per device that loads the library).
 __device__ int g_status_word;
+// Number of O rescales the forward performed while counting was switched on (option
+// "count_rescales"); read with fa_get_option("rescale_events"), cleared by setting it to 0.
+__device__ unsigned long long g_rescale_events;
 
 // Text of the last FA_ERR_CUDA cause on this host thread.
 static thread_local char g_detail[256] = "";
@@ -48,6 +51,23 @@ int* device_status_ptr() {
     e = cudaGetSymbolAddress(&p, g_status_word);
     if (e != cudaSuccess) { cuda_fail("cudaGetSymbolAddress(status word)", e); return nullptr; }
     ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+unsigned long long* rescale_events_ptr() {
+  static unsigned long long* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { cuda_fail("cudaGetDevice", e); return nullptr; }
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_rescale_events);
+    if (e != cudaSuccess) { cuda_fail("cudaGetSymbolAddress(rescale events)", e); return nullptr; }
+    ptrs[dev] = static_cast<unsigned long long*>(p);
   }
   return ptrs[dev];
 }
@@ -160,10 +180,36 @@ int fa_set_option(const char* key, double value) {
     options().poly_exp = static_cast<int>(value);
     return FA_OK;
   }
+  if (!std::strcmp(key, "poly_fraction")) {  // the same split as a fraction of the exponentials
+    if (value == -1.0) { options().poly_exp = -1; return FA_OK; }
+    const double cols = value * 32.0;
+    if (cols != 0.0 && cols != 4.0 && cols != 8.0 && cols != 12.0 && cols != 16.0) return FA_ERR_INVALID_ARG;
+    options().poly_exp = static_cast<int>(cols);
+    return FA_OK;
+  }
   if (!std::strcmp(key, "debug_drop_kv_load")) {
     if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
     options().debug_drop_kv_load = static_cast<int>(value);
     return FA_OK;
+  }
+  if (!std::strcmp(key, "debug_bwd_hook")) {
+    if (value != 0.0 && value != 1.0 && value != 2.0) return FA_ERR_INVALID_ARG;
+    options().debug_bwd_hook = static_cast<int>(value);
+    return FA_OK;
+  }
+  if (!std::strcmp(key, "count_rescales")) {
+    if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+    options().count_rescales = static_cast<int>(value);
+    return FA_OK;
+  }
+  if (!std::strcmp(key, "rescale_events")) {  // only 0: clear the counter (synchronises the device)
+    if (value != 0.0) return FA_ERR_INVALID_ARG;
+    unsigned long long* p = rescale_events_ptr();
+    if (!p) return FA_ERR_CUDA;
+    const unsigned long long zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return e == cudaSuccess ? FA_OK : cuda_fail("clearing the rescale-event counter", e);
   }
   return FA_ERR_INVALID_ARG;
 }
@@ -172,7 +218,23 @@ int fa_get_option(const char* key, double* value) {
   if (!key || !value) return FA_ERR_INVALID_ARG;
   if (!std::strcmp(key, "rescale_threshold")) { *value = options().rescale_threshold; return FA_OK; }
   if (!std::strcmp(key, "poly_exp")) { *value = options().poly_exp; return FA_OK; }
+  if (!std::strcmp(key, "poly_fraction")) {
+    *value = options().poly_exp < 0 ? -1.0 : options().poly_exp / 32.0;
+    return FA_OK;
+  }
   if (!std::strcmp(key, "debug_drop_kv_load")) { *value = options().debug_drop_kv_load; return FA_OK; }
+  if (!std::strcmp(key, "debug_bwd_hook")) { *value = options().debug_bwd_hook; return FA_OK; }
+  if (!std::strcmp(key, "count_rescales")) { *value = options().count_rescales; return FA_OK; }
+  if (!std::strcmp(key, "rescale_events")) {  // synchronises the device, then reads the counter
+    unsigned long long* p = rescale_events_ptr();
+    if (!p) return FA_ERR_CUDA;
+    unsigned long long v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("reading the rescale-event counter", e);
+    *value = static_cast<double>(v);
+    return FA_OK;
+  }
   return FA_ERR_INVALID_ARG;
 }
 
@@ -228,6 +290,8 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.pos_mod = 0;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
+  p.rescale_events = nullptr;
+  if (options().count_rescales && !(p.rescale_events = rescale_events_ptr())) return FA_ERR_CUDA;
   // the exponential-split ablation is built for d = 64 and 128 only
   const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
@@ -318,6 +382,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   p.lse_part = S > 1 ? reinterpret_cast<float*>(ws + ((size_t)S * all_rows * d * 4 + 255) / 256 * 256) : nullptr;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
+  p.rescale_events = nullptr;
+  if (options().count_rescales && !(p.rescale_events = rescale_events_ptr())) return FA_ERR_CUDA;
   // the exponential-split ablation is built for d = 64 and 128 only
   const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -415,6 +481,7 @@ static int bwd_main_impl(const void* q, const void* k, const void* v, const void
   p.scale = scale;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
+  p.debug_hook = options().debug_bwd_hook;
   cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_main launch", e);
 }
@@ -464,10 +531,18 @@ int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d, int determ
   return bwd_post_impl(dq, B, H, N, d, workspace, stream);
 }
 
-int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
-  // validate everything before the first launch
+}  // extern "C"
+
+namespace fa {
+
+// Every check fa_bwd_qk makes, in its order (shapes, options, workspace, pointers, device).
+// Returns FA_OK with *launch set when kernels must run, FA_OK with *launch clear when there is
+// nothing to do (B = 0, or no query row and no key), or the error status.
+int bwd_validate(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 const void* dq, const void* dk, const void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
+                 int causal, float scale, int deterministic, const void* workspace, size_t workspace_bytes,
+                 bool* launch) {
+  *launch = false;
   int st = check_shape(B, H, Hkv, Nk, d);
   if (st) return st;
   st = check_bwd_common(B, H, Hkv, Nq, d, deterministic, workspace, workspace_bytes);
@@ -482,6 +557,25 @@ int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const 
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
+  *launch = true;
+  return FA_OK;
+}
+
+int report_cuda_error(const char* what, cudaError_t e) { return cuda_fail(what, e); }
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate everything before the first launch
+  bool launch = false;
+  int st = bwd_validate(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale, deterministic,
+                        workspace, workspace_bytes, &launch);
+  if (st || !launch) return st;
+  const bool no_queries = Nq == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (no_queries || Nk == 0) {
     // no query row sees a key: the gradients that exist are zero

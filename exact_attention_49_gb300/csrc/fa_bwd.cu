@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(512, 1)
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1;
+        if (p.debug_hook == 2 && t == 1) continue;  // failure-injection test hook (never set in normal use)
         if (!mbar_wait(st_empty(s), ((t >> 1) & 1) ^ 1, abort, p.status)) break;
         const int bh = tile_head(t), i = tile_row(t);
         mbar_arrive_expect_tx(st_full(s), 2 * C::TILE + 1024);
@@ -481,7 +482,8 @@ __global__ void __launch_bounds__(512, 1)
       if (p.deterministic) {
         __threadfence();
         named_bar(1, 128);
-        if (r == 0) st_release(counter, rank + 1);
+        // (failure-injection test hook: the first CTA keeps its successors waiting)
+        if (r == 0 && !(p.debug_hook == 1 && blockIdx.x == 0)) st_release(counter, rank + 1);
       }
     }
     // mma_done is committed after every MMA of the CTA, the last dK one included

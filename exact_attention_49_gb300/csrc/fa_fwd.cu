@@ -308,6 +308,10 @@ __global__ void __launch_bounds__(320, 1)
         const float m_new = need ? m_tile : m_used;
         const float alpha = need ? ex2_mufu(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (p.rescale_events) {  // debug counter: rows whose O is rescaled at this key tile
+            const unsigned moved = __ballot_sync(0xffffffffu, alpha != 1.f);
+            if (lane == 0) atomicAdd(p.rescale_events, (unsigned long long)__popc(moved));
+          }
           // O holds sum_{j'<j} P V against m_used; it must be complete before rescaling
           ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (j - 1) & 1, abort, p.status));
           if (!ok) break;

@@ -13,6 +13,10 @@ struct Options {
   float rescale_threshold = 8.0f;  // tau, log2 units: skip the O/l rescale unless the row max grows by more
   int poly_exp = -1;               // exp2 split: columns of every 32 on the FMA polynomial (0,4,8,12,16; -1 = default)
   int debug_drop_kv_load = 0;      // failure-injection test hook: the forward skips one K/V load
+  int debug_bwd_hook = 0;          // failure-injection test hook of the backward: 1 = the first CTA never
+                                   // releases its deterministic-order counters, 2 = the copy warp skips
+                                   // the second query tile's Q/dO load
+  int count_rescales = 0;          // count the forward's O rescales into the library's event counter
 };
 Options& options();
 
@@ -35,6 +39,7 @@ struct FwdParams {
                      // as rows, pos_mod = Nq); 0: position r + qoff
   float* o_part;     // splits > 1: fp32 [splits][B*H][Nq][d]
   float* lse_part;   // splits > 1: fp32 [splits][B*H][Nq]
+  unsigned long long* rescale_events;  // non-null: add the number of rows whose O was rescaled (per key tile)
 };
 
 struct BwdParams {
@@ -51,6 +56,7 @@ struct BwdParams {
   float scale_log2;   // softmax scale * log2(e)
   float scale;        // softmax scale (folded into dS)
   int* status;        // device status word
+  int debug_hook;     // failure-injection test hook (Options::debug_bwd_hook)
 };
 
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
@@ -77,5 +83,15 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long row
 
 // Device address of the library's status word on the current device (nullptr on error).
 int* device_status_ptr();
+// Every argument check of fa_bwd_qk, in its order; *launch tells whether kernels must run.
+int bwd_validate(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 const void* dq, const void* dk, const void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
+                 int causal, float scale, int deterministic, const void* workspace, size_t workspace_bytes,
+                 bool* launch);
+// Record `what` and CUDA's error text for fa_last_error_detail; returns FA_ERR_CUDA.
+int report_cuda_error(const char* what, cudaError_t e);
+
+// Device address of the library's rescale-event counter on the current device (nullptr on error).
+unsigned long long* rescale_events_ptr();
 
 }  // namespace fa

@@ -23,7 +23,9 @@
 //    threads on one device) race on the array: order them on one stream.
 //  * the first call on each device looks up the array's device address (with
 //    that device current) and caches it; make that first call before any
-//    stream capture.
+//    stream capture.  The cached address belongs to the device's primary
+//    context: calling cudaDeviceReset while the library is loaded is not
+//    supported (the same holds for the library's status word).
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -65,16 +67,19 @@ void* scratch_on_current_device(cudaError_t* err) {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
                               int causal, float scale, int deterministic, void* stream) {
-  // Size checks first, so an oversized or malformed problem touches no GPU state.
-  if (B < 0 || H < 1 || Hkv < 1 || N < 0) return FA_ERR_INVALID_ARG;
-  if (B == 0 || N == 0) return FA_OK;
-  const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d, deterministic);
-  if (need == 0) return (d != 64 && d != 128) ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARG;
-  if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  // fa_bwd's own checks, in its order, with the scratch standing in for the workspace (any
+  // non-null 256-byte aligned address of the scratch's size: only its size and alignment are
+  // checked), so that every status matches fa_bwd's and a rejected call touches no GPU state.
+  bool launch = false;
+  int st = fa::bwd_validate(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, N, d, causal, scale, deterministic,
+                            reinterpret_cast<const void*>(uintptr_t{256}), (size_t)FA_NOALLOC_SCRATCH_BYTES, &launch);
+  if (st || !launch) return st;
   cudaError_t e = cudaSuccess;
   void* ws = scratch_on_current_device(&e);
-  if (!ws) return FA_ERR_CUDA;
+  if (!ws) {
+    cudaGetLastError();  // leave no sticky error behind for the caller's CUDA calls
+    return fa::report_cuda_error("cudaGetSymbolAddress(fa_bwd_noalloc scratch)", e);
+  }
   return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale, deterministic, ws,
                 (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -33,6 +33,11 @@
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  Calls enqueue work and return; they do not synchronise.
  *
+ * Device state.  The library keeps a few words of device memory per device
+ * (status word, event counter, the fa_bwd_noalloc scratch) and caches their
+ * addresses in the device's primary context on first use: calling
+ * cudaDeviceReset while the library is loaded is not supported.
+ *
  * Errors.  Every argument is validated before anything is launched, so a call
  * that returns FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED or
  * FA_ERR_WORKSPACE has not touched the GPU.  FA_ERR_CUDA reports a launch or
@@ -166,7 +171,9 @@ int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d,
  *     serialise them on one stream.
  *   - The first call on a device looks up the array's device address and
  *     caches it; make that first call before any stream capture.
- * Other arguments, checks and status codes are those of fa_bwd. */
+ * Other arguments, checks (in the same order) and status codes are those of
+ * fa_bwd, the scratch taking the workspace's place: FA_ERR_WORKSPACE means
+ * the problem needs more than FA_NOALLOC_SCRATCH_BYTES. */
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                    const float* lse, void* dq, void* dk, void* dv,
                    int B, int H, int Hkv, int N, int d, int causal, float scale, int deterministic,
@@ -182,13 +189,30 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                        polynomial (wiki FA4 (2)) in the forward: number of
  *                        columns out of every 32 computed by the polynomial,
  *                        one of 0, 4, 8, 12, 16; -1 = the built-in default.
+ *   "poly_fraction"      the same split as a fraction of the exponentials:
+ *                        0, 0.125, 0.25, 0.375 or 0.5; -1 = the default.
+ *   "count_rescales"     0 (default) or 1: the forward counts, in a device
+ *                        counter, every (row, key tile) at which it rescaled O
+ *                        (a debug aid that shows the conditional rescale
+ *                        firing or being skipped; one atomic per warp and
+ *                        rescale when on, nothing when off).
+ *   "rescale_events"     the counter: fa_get_option synchronises the device and
+ *                        reads it; fa_set_option(.., 0) synchronises and clears
+ *                        it (any other value is rejected).
  *   "debug_drop_kv_load" failure-injection test hook, 0 (default) or 1: the
  *                        forward's copy warp skips its second K/V tile load, so
  *                        the MMA warp's bounded wait gives up (after ~2 s), the
  *                        CTA drains and exits, and fa_last_device_status()
  *                        returns FA_ERR_DEVICE_TIMEOUT.  Output is undefined
  *                        while it is set.
- * Returns FA_OK or FA_ERR_INVALID_ARG (unknown key or value out of range). */
+ *   "debug_bwd_hook"     failure-injection test hook of the backward, 0
+ *                        (default), 1 (the first CTA never releases the
+ *                        deterministic mode's ordering counters, so the next
+ *                        key tile's bounded spin gives up) or 2 (the copy warp
+ *                        skips the second query tile's Q/dO load, so the MMA
+ *                        warp's bounded wait gives up); then as above.
+ * Returns FA_OK, FA_ERR_INVALID_ARG (unknown key or value out of range) or,
+ * for "rescale_events", FA_ERR_CUDA. */
 int fa_set_option(const char* key, double value);
 int fa_get_option(const char* key, double* value);
 

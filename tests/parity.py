@@ -8,6 +8,14 @@ Tolerances (stated for the hot path):
        keeps 1e-2 as the bound on the computation itself.
   LSE  max-abs error <= 1e-3 (fp32 output).
   dQ, dK, dV  relative Frobenius error ||g - g_oracle|| / ||g_oracle|| <= 2e-2.
+
+Row diagnostic.  A whole-tensor Frobenius norm can hide one wrong row (at
+N = 8192 a fully wrong row adds about 1% to it), so the gradient tests also log
+the worst row: max_r ||g_r - g_oracle_r|| / rms_r ||g_oracle_r|| (rows of dQ are
+queries, rows of dK, dV are keys; the denominator is the root-mean-square row
+norm, so rows whose exact gradient is near zero, such as the first causal
+query's dQ, do not blow it up).  A row that is wrong as a whole scores about 1;
+the tests require <= ROW_TOL.
 """
 from __future__ import annotations
 
@@ -19,6 +27,7 @@ import numpy as np
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_RTOL = 2e-2
+ROW_TOL = 0.25
 
 
 def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
@@ -50,6 +59,18 @@ def rel_fro(g, g_ref) -> float:
     g_ref = np.asarray(g_ref, np.float64)
     den = np.linalg.norm(g_ref)
     return float(np.linalg.norm(g - g_ref) / (den if den > 0 else 1.0))
+
+
+def row_err(g, g_ref) -> float:
+    """Worst row error relative to the RMS row norm of g_ref (rows = all axes but the last)."""
+    g = np.asarray(g, np.float64)
+    g_ref = np.asarray(g_ref, np.float64)
+    if g_ref.size == 0:
+        return 0.0
+    d = g_ref.shape[-1]
+    diff = np.linalg.norm((g - g_ref).reshape(-1, d), axis=1)
+    rms = float(np.sqrt(np.mean(np.sum(g_ref.reshape(-1, d) ** 2, axis=1))))
+    return float(diff.max() / (rms if rms > 0 else 1.0))
 
 
 def to64(t) -> np.ndarray:

@@ -61,6 +61,38 @@ def test_options_roundtrip(L):
     assert fa.fa_set_option("no_such_option", 1.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_option("debug_drop_kv_load", 2) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_get_option("debug_drop_kv_load") == 0.0
+    # the exponential split as a fraction of the exponentials (columns of 32 / 32)
+    for frac, cols in ((0.0, 0), (0.125, 4), (0.25, 8), (0.375, 12), (0.5, 16)):
+        assert fa.fa_set_option("poly_fraction", frac) == fa.FA_OK
+        assert fa.fa_get_option("poly_exp") == cols
+        assert fa.fa_get_option("poly_fraction") == frac
+    assert fa.fa_set_option("poly_fraction", 0.3) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_option("poly_fraction", -1) == fa.FA_OK
+    assert fa.fa_get_option("poly_exp") == -1
+    for key, good, bad in (("debug_bwd_hook", (0, 1, 2), (3, -1, 0.5)), ("count_rescales", (0, 1), (2, 0.5))):
+        for val in good:
+            assert fa.fa_set_option(key, val) == fa.FA_OK
+            assert fa.fa_get_option(key) == val
+        for val in bad:
+            assert fa.fa_set_option(key, val) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_set_option(key, 0) == fa.FA_OK
+    # the event counter can only be cleared (to 0), and only with a device
+    assert fa.fa_set_option("rescale_events", 5) == fa.FA_ERR_INVALID_ARG
+
+
+def test_row_diagnostic_catches_one_wrong_row():
+    """The per-row gradient diagnostic of the parity tests: rounding-size noise scores far
+    below its bound, one row replaced by another row's values scores about 1."""
+    import numpy as np
+    from parity import ROW_TOL, rel_fro, row_err
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((1, 2, 8192, 128))
+    noisy = ref * (1 + 2.0 ** -8 * rng.standard_normal(ref.shape))
+    assert row_err(noisy, ref) < 0.05 * ROW_TOL
+    bad = noisy.copy()
+    bad[0, 1, 4000] = ref[0, 1, 17]
+    assert rel_fro(bad, ref) < 0.02          # hidden by the whole-tensor norm
+    assert row_err(bad, ref) > 4 * ROW_TOL   # caught by the row diagnostic
 
 
 P = ctypes.c_void_p
@@ -210,3 +242,33 @@ int use_fa(void* q, void* k, void* v, void* o, float* lse, void* ws, size_t wsb)
                           "-I", os.path.join(ROOT, "include"), "-o", str(tmp_path / "use_fa.o")],
                          capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
+
+
+def test_noalloc_validates_like_fa_bwd(L):
+    """fa_bwd_noalloc makes fa_bwd's checks in fa_bwd's order (the scratch standing in for the
+    workspace), so both give the same status on every rejected call; none of these touches
+    the GPU."""
+    L.fa_bwd_noalloc.restype = ctypes.c_int
+    L.fa_bwd_noalloc.argtypes = [P] * 9 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, P]
+    big_ws = 1 << 40  # any size: the checks below fail before the workspace size matters
+    cases = [
+        dict(d=96, N=0),                 # unsupported d even with no rows
+        dict(d=256, N=128),              # no backward at d = 256
+        dict(H=3, Hkv=2),                # H % Hkv != 0
+        dict(det=2),                     # bad deterministic flag
+        dict(causal=2),                  # bad causal flag
+        dict(scale=float("nan")),        # bad scale
+        dict(q=None),                    # null pointer
+        dict(k=BAD),                     # misaligned pointer
+    ]
+    for c in cases:
+        a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, do=GOOD, lse=GOOD, dq=GOOD, dk=GOOD, dv=GOOD, B=1, H=2, Hkv=1,
+                 N=128, d=64, causal=0, scale=0.125, det=0)
+        a.update(c)
+        ptrs = [a[n] for n in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv")]
+        sizes = (a["B"], a["H"], a["Hkv"], a["N"], a["d"], a["causal"])
+        want = L.fa_bwd(*ptrs, *sizes, a["scale"], a["det"], GOOD, big_ws, None)
+        got = L.fa_bwd_noalloc(*ptrs, *sizes, a["scale"], a["det"], None)
+        assert want != 0 and got == want, (c, got, want)
+    # nothing to do: both return FA_OK without touching the GPU
+    assert L.fa_bwd_noalloc(*([GOOD] * 9), 0, 2, 1, 128, 64, 0, 0.125, 0, None) == 0

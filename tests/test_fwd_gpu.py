@@ -150,3 +150,34 @@ def test_fwd_exp2_split(poly):
         check_full(2, 4, 2, 640, 64, False, seed=43)
     finally:
         fa.fa_set_option("poly_exp", old)
+
+
+def _rescale_events(B, H, N, d, causal, seed, qk_mult, tau):
+    """Rows x key tiles at which the forward rescaled O (the library's debug counter)."""
+    old_tau = fa.fa_get_option("rescale_threshold")
+    try:
+        assert fa.fa_set_option("rescale_threshold", tau) == fa.FA_OK
+        assert fa.fa_set_option("count_rescales", 1) == fa.FA_OK
+        assert fa.fa_set_option("rescale_events", 0) == fa.FA_OK
+        check_full(B, H, H, N, d, causal, seed=seed, qk_mult=qk_mult)
+        return int(fa.fa_get_option("rescale_events"))
+    finally:
+        fa.fa_set_option("count_rescales", 0)
+        fa.fa_set_option("rescale_threshold", old_tau)
+
+
+def test_fwd_conditional_rescale_events():
+    """The conditional rescale really skips and really fires: on inputs with Q, K x4 (scores
+    spread over ~16x the usual range) the O correction runs at tau = 8, more often at tau = 0
+    (every growth of the row max), and never at tau = 64 on unscaled inputs, where the row max
+    moves by far less than 2^64 after the first key tile; the results stay within tolerance in
+    every case (checked by check_full)."""
+    ev8 = _rescale_events(1, 4, 2048, 128, True, 11, 4.0, 8.0)
+    ev0 = _rescale_events(1, 4, 2048, 128, True, 11, 4.0, 0.0)
+    ev64 = _rescale_events(1, 4, 2048, 128, True, 11, 1.0, 64.0)
+    ev0_plain = _rescale_events(1, 4, 2048, 128, True, 11, 1.0, 0.0)
+    record("fwd_rescale_events", tau8_x4=ev8, tau0_x4=ev0, tau64=ev64, tau0=ev0_plain)
+    assert ev8 > 0
+    assert ev0 > ev8
+    assert ev0_plain > 0
+    assert ev64 == 0

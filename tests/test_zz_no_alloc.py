@@ -39,7 +39,7 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("d,causal,det", [(64, True, 0), (128, True, 0), (128, False, 1)])
+@pytest.mark.parametrize("d,causal,det", [(64, True, 0), (128, True, 0), (128, False, 1), (128, True, 1)])
 def test_noalloc_matches_fa_bwd_twice(noalloc, d, causal, det):
     B, H, Hkv, N = 2, 4, 2, 512
     scale = d ** -0.5
@@ -60,6 +60,28 @@ def test_noalloc_matches_fa_bwd_twice(noalloc, d, causal, det):
             assert rel_fro(to64(got), to64(want)) <= GRAD_RTOL
             if det:
                 assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_noalloc_large_then_small_problem(noalloc):
+    """The scratch keeps whatever the previous call left in it; a smaller problem after a
+    larger one (deterministic, so the ordering counters are reused too) must still match
+    fa_bwd bit for bit."""
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for B, H, Hkv, N in ((2, 8, 2, 1024), (1, 2, 1, 384)):
+        d, causal = 128, True
+        scale = d ** -0.5
+        assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, 1) <= SCRATCH_BYTES
+        q, k, v, do = (t.cuda() for t in make_inputs(B, H, Hkv, N, d, seed=40 + N))
+        o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale)
+        want = fa.attention_backward(q, k, v, o, do, lse, causal=causal, scale=scale, deterministic=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        st = noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                     B, H, Hkv, N, d, int(causal), scale, 1, stream)
+        assert st == fa.FA_OK, fa.status_string(st)
+        torch.cuda.synchronize()
+        assert fa.fa_last_device_status() == fa.FA_OK
+        for got, ref_t in zip((dq, dk, dv), want):
+            assert torch.equal(got.view(torch.int16), ref_t.view(torch.int16))
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(noalloc):
