@@ -269,6 +269,8 @@ def run_ours(args, w):
     fwd_only = args.fwd_only or not w.backward
     if args.poly_exp is not None and fa.fa_set_option("poly_exp", args.poly_exp) != fa.FA_OK:
         raise SystemExit("bad --poly-exp %r" % args.poly_exp)
+    if args.bwd_2cta is not None and fa.fa_set_option("bwd_2cta", args.bwd_2cta) != fa.FA_OK:
+        raise SystemExit("bad --bwd-2cta %r" % args.bwd_2cta)
     ws_bytes = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, det)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -405,6 +407,7 @@ def run_ours(args, w):
                                                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": (1 if fwd_only else 4) * args.steps,
         "poly_exp": fa.fa_get_option("poly_exp"),
+        "bwd_2cta": fa.fa_get_option("bwd_2cta"),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -513,6 +516,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true", help="time the forward alone")
     ap.add_argument("--poly-exp", type=int, default=None, help="exp2 split: columns of 32 on the FMA polynomial")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--bwd-2cta", type=int, default=None, choices=[0, 1],
+                    help="backward main stage on CTA pairs (1) or one CTA per key tile (0); default: library's")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -49,6 +50,40 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _sources() + _headers() + [__file__])
 
 
+def ptxas_report(text: str) -> dict:
+    """Per kernel (mangled name): registers, spill stores and spill loads, from ptxas -v output."""
+    out = {}
+    cur = None
+    for line in text.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = m.group(1)
+            out[cur] = {"registers": None, "spill_stores": 0, "spill_loads": 0}
+            continue
+        if cur is None:
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m:
+            out[cur]["spill_stores"], out[cur]["spill_loads"] = int(m.group(1)), int(m.group(2))
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            out[cur]["registers"] = int(m.group(1))
+    return out
+
+
+# The forward kernel splits its registers between warpgroups with setmaxnreg, assuming it is
+# launched at exactly this many registers per thread (FwdCfg::REG_LAUNCH): an increase beyond
+# what the launch holds would wait forever, so the build refuses any other count.
+FWD_LAUNCH_REGISTERS = 168
+
+
+def check_register_split(report: dict) -> None:
+    for name, r in report.items():
+        if "fwd_kernel" in name and r["registers"] != FWD_LAUNCH_REGISTERS:
+            raise RuntimeError("%s compiled at %s registers per thread, not %d: the setmaxnreg split of the "
+                               "forward kernel would not add up" % (name, r["registers"], FWD_LAUNCH_REGISTERS))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link the library if any source is newer than it; return its path."""
     if not force and not _stale():
@@ -75,6 +110,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join("%s:\n%s" % (s, t[-4000:]) for s, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
+    check_register_split(ptxas_report("\n".join(log)))
     tmp = LIB + ".tmp.%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     subprocess.run(cmd, check=True)

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -20,6 +21,9 @@ __device__ int g_status_word;
 // Number of O rescales the forward performed while counting was switched on (option
 // "count_rescales"); read with fa_get_option("rescale_events"), cleared by setting it to 0.
 __device__ unsigned long long g_rescale_events;
+// Kernel-wide abort word: a launch whose CTA gives up a wait stores its generation here so the
+// launch's other CTAs stop waiting too (see Abort in sm103.cuh).
+__device__ unsigned g_abort_word;
 
 // Text of the last FA_ERR_CUDA cause on this host thread.
 static thread_local char g_detail[256] = "";
@@ -72,6 +76,30 @@ unsigned long long* rescale_events_ptr() {
   return ptrs[dev];
 }
 
+unsigned* abort_word_ptr() {
+  static unsigned* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { cuda_fail("cudaGetDevice", e); return nullptr; }
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_abort_word);
+    if (e != cudaSuccess) { cuda_fail("cudaGetSymbolAddress(abort word)", e); return nullptr; }
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+unsigned next_generation() {
+  static std::atomic<unsigned> g{0};
+  unsigned v = ++g;
+  if (v == 0) v = ++g;  // 0 is the word's initial value: never a launch's generation
+  return v;
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -87,12 +115,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer) {
+int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return -1;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)outer};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -202,6 +230,11 @@ int fa_set_option(const char* key, double value) {
     options().count_rescales = static_cast<int>(value);
     return FA_OK;
   }
+  if (!std::strcmp(key, "bwd_2cta")) {
+    if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+    options().bwd_2cta = static_cast<int>(value);
+    return FA_OK;
+  }
   if (!std::strcmp(key, "rescale_events")) {  // only 0: clear the counter (synchronises the device)
     if (value != 0.0) return FA_ERR_INVALID_ARG;
     unsigned long long* p = rescale_events_ptr();
@@ -225,6 +258,7 @@ int fa_get_option(const char* key, double* value) {
   if (!std::strcmp(key, "debug_drop_kv_load")) { *value = options().debug_drop_kv_load; return FA_OK; }
   if (!std::strcmp(key, "debug_bwd_hook")) { *value = options().debug_bwd_hook; return FA_OK; }
   if (!std::strcmp(key, "count_rescales")) { *value = options().count_rescales; return FA_OK; }
+  if (!std::strcmp(key, "bwd_2cta")) { *value = options().bwd_2cta; return FA_OK; }
   if (!std::strcmp(key, "rescale_events")) {  // synchronises the device, then reads the counter
     unsigned long long* p = rescale_events_ptr();
     if (!p) return FA_ERR_CUDA;
@@ -292,6 +326,8 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (!p.status) return FA_ERR_CUDA;
   p.rescale_events = nullptr;
   if (options().count_rescales && !(p.rescale_events = rescale_events_ptr())) return FA_ERR_CUDA;
+  if (!(p.kabort = abort_word_ptr())) return FA_ERR_CUDA;
+  p.gen = next_generation();
   // the exponential-split ablation is built for d = 64 and 128 only
   const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
@@ -384,6 +420,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   if (!p.status) return FA_ERR_CUDA;
   p.rescale_events = nullptr;
   if (options().count_rescales && !(p.rescale_events = rescale_events_ptr())) return FA_ERR_CUDA;
+  if (!(p.kabort = abort_word_ptr())) return FA_ERR_CUDA;
+  p.gen = next_generation();
   // the exponential-split ablation is built for d = 64 and 128 only
   const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -482,7 +520,18 @@ static int bwd_main_impl(const void* q, const void* k, const void* v, const void
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.debug_hook = options().debug_bwd_hook;
-  cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  if (!(p.kabort = abort_word_ptr())) return FA_ERR_CUDA;
+  p.gen = next_generation();
+  cudaError_t e;
+  if (d == 128 && options().bwd_2cta) {
+    CUtensorMap tq64, tdo64;
+    if (make_tmap_bf16_rows(&tq64, q, d, Nq, (long long)B * H, 64) ||
+        make_tmap_bf16_rows(&tdo64, dout, d, Nq, (long long)B * H, 64))
+      return FA_ERR_CUDA;
+    e = launch_bwd_main_pair(tq, tq64, tk, tv, tdo, tdo64, p, static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_bwd_main(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_main launch", e);
 }
 

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t mma_done = bar0 + 8u * 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const Abort ab{abort, p.status, p.kabort, p.gen};
 
   // ---- work unit
   const int N = p.Nq;  // query rows; keys: p.Nk
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1;
         if (p.debug_hook == 2 && t == 1) continue;  // failure-injection test hook (never set in normal use)
-        if (!mbar_wait(st_empty(s), ((t >> 1) & 1) ^ 1, abort, p.status)) break;
+        if (!mbar_wait(st_empty(s), ((t >> 1) & 1) ^ 1, ab)) break;
         const int bh = tile_head(t), i = tile_row(t);
         mbar_arrive_expect_tx(st_full(s), 2 * C::TILE + 1024);
         for (int ch = 0; ch < C::CHUNKS; ++ch) {
@@ -246,8 +247,8 @@ __global__ void __launch_bounds__(512, 1)
     auto sQ = [&](int s) { return sbase + C::OFF_Q + s * C::TILE; };
     auto sDO = [&](int s) { return sbase + C::OFF_DO + s * C::TILE; };
     bool ok = ntiles > 0;
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, p.status));
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(st_full(0), 0, abort, p.status));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, ab));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(st_full(0), 0, ab));
     if (ok) {
       tc_fence_after();
       ss_kmajor(C::COL_S, sK, sQ(0));
@@ -260,16 +261,16 @@ __global__ void __launch_bounds__(512, 1)
     auto step = [&](int t, auto more_tiles) -> bool {
       constexpr bool MORE = decltype(more_tiles)::value;
       const int s = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, abort, p.status))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(p_ready, t & 1, ab))) return false;
       tc_fence_after();
       ts_acc(C::COL_DV, C::COL_S, sDO(s), t > 0);  // dV += P^T dO_t
       if constexpr (MORE) {
-        if (!__all_sync(0xffffffffu, mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, abort, p.status))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(st_full(s ^ 1), ((t + 1) >> 1) & 1, ab))) return false;
         tc_fence_after();
         ss_kmajor(C::COL_S, sK, sQ(s ^ 1));  // S^T of the next tile (P^T_t already consumed)
         mma_commit(s_full, leader);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(ds_ready, t & 1, abort, p.status))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(ds_ready, t & 1, ab))) return false;
       tc_fence_after();
       // dQ first, so its read-out overlaps the dK MMA
       if constexpr (C::DQ_T) {
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(512, 1)
                sdesc_sw128(sQ(s) + kk * 2048, 16384, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u, leader);
       mma_commit(st_empty(s), leader);
       if constexpr (MORE) {
-        if (!__all_sync(0xffffffffu, mbar_wait(dq_empty, t & 1, abort, p.status))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(dq_empty, t & 1, ab))) return false;
         tc_fence_after();
         ss_kmajor(C::COL_DP, sV, sDO(s ^ 1));
         mma_commit(dp_full, leader);
@@ -303,8 +304,15 @@ __global__ void __launch_bounds__(512, 1)
     };
     for (int t = 0; ok && t + 1 < ntiles; ++t) ok = step(t, std::true_type{});
     if (ok && ntiles > 0) ok = step(ntiles - 1, std::false_type{});
+    // drain: every MMA issued above has finished before TMEM is released (bounded, and
+    // waited for even after an abort)
     mma_commit(mma_done, leader);
-    __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
+    {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(mma_done, 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ compute: P^T and dS^T
     const int w = warp >> 2;           // query-column half
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(512, 1)
       // this half's 64 queries: lse2 and D, four per 16-byte shared load
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024) + 16 * w;
       const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 1024 + 512) + 16 * w;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, ab))) break;
       tc_fence_after();
       float pv[64];
       {
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       mbar_arrive(p_ready);
 
-      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, abort, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, ab))) break;
       tc_fence_after();
       {
         uint32_t ra[32], rb[32];
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int bh = tile_head(t), i = tile_row(t);
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, ab));
       if (!ok) break;
       tc_fence_after();
       int* counter = p.deterministic ? p.counters + ((size_t)bh * nq + i) : nullptr;
@@ -426,9 +434,10 @@ __global__ void __launch_bounds__(512, 1)
         if (r == 0) {
           const uint64_t t0 = globaltimer();
           while (ld_acquire(counter) != rank) {
-            if (*abort || globaltimer() - t0 > kWaitLimitNs) {
-              *abort = 1;
-              atomicCAS(p.status, 0, kStatusTimeout);
+            const unsigned long long el = globaltimer() - t0;
+            if (should_stop(ab, el)) break;
+            if (el > kWaitLimitNs) {
+              give_up(ab);
               break;
             }
           }
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     // mma_done is committed after every MMA of the CTA, the last dK one included
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, abort, p.status));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, ab));
     if (ok) {
       tc_fence_after();
       const size_t krow = (size_t)bg * p.Nk + (size_t)j * 128 + r;

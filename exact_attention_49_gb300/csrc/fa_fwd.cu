@@ -46,25 +46,78 @@ struct FwdCfg {
   static constexpr int BN = 128;                    // keys per K/V tile
   static constexpr int TILE = 128 * D * 2;          // bytes of one 128 x D bf16 tile
   static constexpr int CHUNKS = D / 64;             // 128-byte swizzle atoms across D
-  // query tiles per CTA: two (S0 | S1 | O0 | O1 in TMEM), or one at d = 256 (S0 | O0 already
-  // take 384 of the 512 columns)
+  // query tiles per work unit: two (S0 | S1 | O0 | O1 in TMEM), or one at d = 256 (S0 | O0
+  // already take 384 of the 512 columns)
   static constexpr int NT = (D == 256) ? 1 : 2;
-  static constexpr int BLOCK = 128 * NT;            // query rows per CTA
+  static constexpr int BLOCK = 128 * NT;            // query rows per work unit
   static constexpr int STAGES = (D == 256) ? 2 : (D == 128) ? 4 : 8;  // K/V ring slots
   static constexpr int SMEM_Q = NT * TILE;
   static constexpr int SMEM_RING = STAGES * TILE;
-  static constexpr int NBAR = 2 * STAGES + 8;
+  static constexpr int NBAR = 2 * STAGES + 11;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = (NT == 2) ? 256 : 128, COL_O1 = 256 + D;
+  // Register split (setmaxnreg): the kernel is launched at 168 registers per thread (384
+  // threads, 64512 registers); the two softmax warpgroups take 224 each, the copy/MMA
+  // warpgroup keeps 56.  The shares must add up to the launch's total, or the increase waits
+  // forever (build.py checks the compiled register count).
+  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 184, REG_OTHER = 136;
+  static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER == THREADS * REG_LAUNCH, "register split");
 };
+
+// One work unit: a block of BLOCK query rows of one (b, h) and, with split-KV, a key range.
+struct FwdUnit {
+  int bh, q0, j0, n_kv, kv_z;
+  int sp;    // key-range split (0 when splits = 1)
+  bool two;  // the block has rows in query tile 1
+};
+
+// Units are numbered heaviest first under a causal mask (the blocks nearest the end of the
+// sequence see the most keys), then by (b, h), then by split.
+template <int D>
+FA_DEV FwdUnit fwd_unit(const FwdParams& p, int u) {
+  using C = FwdCfg<D>;
+  const int N = p.Nq;  // query rows; keys: p.Nk
+  const int ncb = (N + C::BLOCK - 1) / C::BLOCK;
+  const int BH = p.B * p.H;
+  FwdUnit w;
+  w.sp = u % p.splits;
+  const int t = u / p.splits;
+  const int cb = p.causal ? (ncb - 1 - t / BH) : (t / BH);
+  w.bh = t % BH;
+  const int b = w.bh / p.H, h = w.bh % p.H;
+  const int g = h / (p.H / p.Hkv);
+  w.q0 = cb * C::BLOCK;
+  const int n_kv_all = (p.Nk + 127) / 128;
+  // causal: the block's last row (position row + qoff) bounds the key tiles it needs; a block
+  // whose rows see no key at all still runs one fully masked tile (O = 0, LSE = -inf)
+  const int last_row = min(w.q0 + C::BLOCK - 1, N - 1);
+  const int k_last = (p.pos_mod ? min(last_row, p.pos_mod - 1) : last_row) + p.qoff;
+  const int n_vis = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
+  // this unit's key tiles [j0, j0 + n_kv); a split whose range holds no visible key still runs
+  // one fully masked tile, which gives O = 0 and LSE = -inf for it
+  w.j0 = w.sp * p.split_tiles;
+  w.n_kv = max(1, min(n_vis, w.j0 + p.split_tiles) - w.j0);
+  // a block with at most 128 rows (a ragged last block; decoding) runs query tile 0 only
+  w.two = C::NT == 2 && N - w.q0 > 128;
+  w.kv_z = b * p.Hkv + g;
+  return w;
+}
+
+// The r-th unit of this CTA: one CTA per SM walks the units in boustrophedon order (row r of
+// gridDim.x units left to right when r is even, right to left when odd), which balances the
+// heaviest-first causal costs across CTAs to within about 1% on large problems.
+FA_DEV int fwd_unit_index(int r) {
+  const int G = gridDim.x;
+  return r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+}
 
 // POLY: how many of every 16 column pairs take the FMA-pipe polynomial exp2 instead of
 // the MUFU ex2 unit (0 = MUFU only).
 template <int D, int POLY>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_units) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,40 +128,19 @@ __global__ void __launch_bounds__(320, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
   const uint32_t q_full = bar0 + 8u * (2 * C::STAGES);
-  auto s_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 1 + w); };
-  auto p_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 3 + w); };
-  auto o_bar = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 5 + w); };
-  const uint32_t mma_done = bar0 + 8u * (2 * C::STAGES + 7);
+  const uint32_t q_empty = bar0 + 8u * (2 * C::STAGES + 1);
+  auto s_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 2 + w); };
+  auto p_full = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 4 + w); };
+  auto o_bar = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 6 + w); };
+  auto o_free = [&](int w) { return bar0 + 8u * (2 * C::STAGES + 8 + w); };
+  const uint32_t mma_done = bar0 + 8u * (2 * C::STAGES + 10);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const Abort ab{abort, p.status, p.kabort, p.gen};
 
   const int warp = warp_id();
   const int lane = lane_id();
-
-  // ---- work unit: (b, h, block of 256 query rows); causal: heaviest blocks first
-  const int N = p.Nq;  // query rows; keys: p.Nk
-  const int ncb = (N + C::BLOCK - 1) / C::BLOCK;
-  const int BH = p.B * p.H;
-  const int sp = blockIdx.x % p.splits;  // key-range split (split-KV); 0 when splits = 1
-  const int t = blockIdx.x / p.splits;
-  const int cb = p.causal ? (ncb - 1 - t / BH) : (t / BH);
-  const int bh = t % BH;
-  const int b = bh / p.H, h = bh % p.H;
-  const int g = h / (p.H / p.Hkv);
-  const int q0 = cb * C::BLOCK;
-  const int n_kv_all = (p.Nk + 127) / 128;
-  // causal: the block's last row (position row + qoff) bounds the key tiles it needs; a block
-  // whose rows see no key at all still runs one fully masked tile (O = 0, LSE = -inf)
-  const int last_row = min(q0 + C::BLOCK - 1, N - 1);
-  const int k_last = (p.pos_mod ? min(last_row, p.pos_mod - 1) : last_row) + p.qoff;
-  const int n_vis = p.causal ? (k_last < 0 ? 1 : min(n_kv_all, k_last / 128 + 1)) : n_kv_all;
-  // this CTA's key tiles [j0, j0 + n_kv); a split whose range holds no visible key still runs
-  // one fully masked tile, which gives O = 0 and LSE = -inf for it
-  const int j0 = sp * p.split_tiles;
-  const int n_kv = max(1, min(n_vis, j0 + p.split_tiles) - j0);
-  // a block with at most 128 rows (a ragged last block; decoding) runs query tile 0 only
-  const bool two = C::NT == 2 && N - q0 > 128;
-  const int kv_z = b * p.Hkv + g;
+  const int N = p.Nq;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -116,10 +148,12 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int w = 0; w < 2; ++w) {
       mbar_init(s_full(w), 1);
       mbar_init(p_full(w), 128);
       mbar_init(o_bar(w), 1);
+      mbar_init(o_free(w), 128);
     }
     mbar_init(mma_done, 1);
     *abort = 0;
@@ -139,40 +173,55 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
-      for (int qt = 0; qt < C::NT; ++qt)
-        for (int ch = 0; ch < C::CHUNKS; ++ch)
-          tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, q0 + qt * 128, bh);
-      int issued = 0;
-      for (int it = 0; it < 2 * n_kv; ++it) {
-        const int slot = it % C::STAGES;
-        if (it == p.drop_it) continue;  // failure-injection test hook (never set in normal use)
-        if (!mbar_wait(empty_bar(slot), ((it / C::STAGES) & 1) ^ 1, abort, p.status)) break;
-        mbar_arrive_expect_tx(full_bar(slot), C::TILE);
-        for (int ch = 0; ch < C::CHUNKS; ++ch)
-          tma_load_3d(smem_u32(sRing + slot * C::TILE + ch * 16384), (it & 1) ? &tm_v : &tm_k, full_bar(slot),
-                      ch * 64, (j0 + (it >> 1)) * 128, kv_z);
-        issued = it + 1;
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+    if (warp == 9 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
+      int it = 0;        // ring position of the next K/V load (continues across units)
+      int issued = 0;    // ring loads issued
+      int q_loads = 0;   // Q loads issued (one per unit)
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = fwd_unit_index(r);
+        if (u >= n_units) break;
+        const FwdUnit w = fwd_unit<D>(p, u);
+        // the Q buffer is free once the previous unit's last S MMAs have completed
+        if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, ab)) break;
+        mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
+        for (int qt = 0; qt < C::NT; ++qt)
+          for (int ch = 0; ch < C::CHUNKS; ++ch)
+            tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, w.q0 + qt * 128, w.bh);
+        ++q_loads;
+        for (int jj = 0; jj < 2 * w.n_kv; ++jj, ++it) {
+          const int slot = it % C::STAGES;
+          if (r == 0 && jj == p.drop_it) continue;  // failure-injection test hook (never set in normal use)
+          if (!mbar_wait(empty_bar(slot), ((it / C::STAGES) & 1) ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(slot), C::TILE);
+          for (int ch = 0; ch < C::CHUNKS; ++ch)
+            tma_load_3d(smem_u32(sRing + slot * C::TILE + ch * 16384), (jj & 1) ? &tm_v : &tm_k, full_bar(slot),
+                        ch * 64, (w.j0 + (jj >> 1)) * 128, w.kv_z);
+          issued = it + 1;
+        }
       }
       if (*abort) {
-        // The CTA gave up: let the copies still in flight land before the CTA
-        // exits (each completes its slot's phase), bounded at 1 ms per copy.
-        for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+        // The CTA gave up: let the copies still in flight land before the CTA exits (each
+        // completes its slot's phase), bounded at 1 ms per copy.
+        for (int k = max(0, issued - C::STAGES); k < issued; ++k) {
           const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(full_bar(it % C::STAGES), (it / C::STAGES) & 1) && globaltimer() - t0 < 1000000ull) {
+          while (!mbar_try_wait(full_bar(k % C::STAGES), (k / C::STAGES) & 1) && globaltimer() - t0 < 1000000ull) {
           }
         }
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(q_full, 0) && globaltimer() - t0 < 1000000ull) {
+        if (q_loads > 0) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(q_full, (q_loads - 1) & 1) && globaltimer() - t0 < 1000000ull) {
+          }
         }
       }
-    }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
       const uint32_t q_addr = smem_u32(sQ);
@@ -194,45 +243,57 @@ __global__ void __launch_bounds__(320, 1)
           mma_ts(tmem + (w ? C::COL_O1 : C::COL_O0), tmem + sc + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
                  idO, (acc || kk > 0) ? 1u : 0u);
       };
-      auto slot_of = [&](int it) { return it % C::STAGES; };
-      auto par_of = [&](int it) { return (uint32_t)((it / C::STAGES) & 1); };
-      // The key-tile loop, compiled once for two query tiles and once for one: a run-time
-      // branch on the tile count inside this one-lane issue loop costs about 1% of the kernel.
-      auto mma_loop = [&](auto two_tiles) {
+      auto slot_of = [&](int k) { return k % C::STAGES; };
+      auto par_of = [&](int k) { return (uint32_t)((k / C::STAGES) & 1); };
+      int it = 0;            // ring position (continues across units)
+      int units = 0;         // units issued (q_full phase, o_free(0) phase)
+      int units2 = 0;        // two-tile units issued (o_free(1) phase)
+      int jg0 = 0, jg1 = 0;  // key tiles issued per query tile (p_full phases)
+      // One unit's MMAs, compiled once for two query tiles and once for one: a run-time branch
+      // on the tile count inside this one-lane issue loop costs about 1% of the kernel.
+      auto unit_mma = [&](const FwdUnit& w, auto two_tiles) -> bool {
         constexpr bool TWO = decltype(two_tiles)::value;
-        bool ok = mbar_wait(q_full, 0, abort, p.status);
-        if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), abort, p.status);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, slot_of(0));
-          mma_commit(s_full(0));
-          if constexpr (TWO) {
-            issue_s(1, slot_of(0));
-            mma_commit(s_full(1));
-          }
-          mma_commit(empty_bar(slot_of(0)));
+        if (!mbar_wait(q_full, units & 1, ab)) return false;
+        if (!mbar_wait(full_bar(slot_of(it)), par_of(it), ab)) return false;
+        tc_fence_after();
+        issue_s(0, slot_of(it));
+        mma_commit(s_full(0));
+        if constexpr (TWO) {
+          issue_s(1, slot_of(it));
+          mma_commit(s_full(1));
         }
-        // one key tile; MORE: another tile follows (the last iteration is peeled so that
-        // neither test is a run-time branch of the issue loop)
+        if (w.n_kv == 1) mma_commit(q_empty);  // the unit's last S MMAs: the Q buffer frees after them
+        mma_commit(empty_bar(slot_of(it)));
+        // The first PV of a query tile overwrites its O accumulator, which the softmax warps
+        // of the previous unit may still be reading out; they release it before they start on
+        // this unit's first exponentials, so this wait rarely stalls.
+        if (units > 0 && !mbar_wait(o_free(0), (units - 1) & 1, ab)) return false;
+        if constexpr (TWO) {
+          if (units2 > 0 && !mbar_wait(o_free(1), (units2 - 1) & 1, ab)) return false;
+        }
+        // one key tile; MORE: another tile follows (the last iteration is peeled so that the
+        // test is not a run-time branch of the issue loop)
         auto step = [&](int j, auto more_tiles) -> bool {
           constexpr bool MORE = decltype(more_tiles)::value;
-          const int itv = 2 * j + 1, itk = 2 * j + 2;
-          if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), abort, p.status)) return false;
-          if (!mbar_wait(p_full(0), j & 1, abort, p.status)) return false;
+          const int itv = it + 2 * j + 1, itk = it + 2 * j + 2;
+          if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), ab)) return false;
+          if (!mbar_wait(p_full(0), jg0 & 1, ab)) return false;
           tc_fence_after();
           issue_pv(0, slot_of(itv), j > 0);
           mma_commit(o_bar(0));
+          ++jg0;
           if constexpr (MORE) {
-            if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), abort, p.status)) return false;
+            if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), ab)) return false;
             tc_fence_after();
             issue_s(0, slot_of(itk));
             mma_commit(s_full(0));
           }
           if constexpr (TWO) {
-            if (!mbar_wait(p_full(1), j & 1, abort, p.status)) return false;
+            if (!mbar_wait(p_full(1), jg1 & 1, ab)) return false;
             tc_fence_after();
             issue_pv(1, slot_of(itv), j > 0);
             mma_commit(o_bar(1));
+            ++jg1;
           }
           mma_commit(empty_bar(slot_of(itv)));
           if constexpr (MORE) {
@@ -240,139 +301,165 @@ __global__ void __launch_bounds__(320, 1)
               issue_s(1, slot_of(itk));
               mma_commit(s_full(1));
             }
+            if (j + 2 == w.n_kv) mma_commit(q_empty);
             mma_commit(empty_bar(slot_of(itk)));
           }
           return true;
         };
-        for (int j = 0; ok && j + 1 < n_kv; ++j) ok = step(j, std::true_type{});
-        if (ok) step(n_kv - 1, std::false_type{});
+        bool ok = true;
+        for (int j = 0; ok && j + 1 < w.n_kv; ++j) ok = step(j, std::true_type{});
+        if (ok) ok = step(w.n_kv - 1, std::false_type{});
+        it += 2 * w.n_kv;
+        return ok;
       };
-      if (two)
-        mma_loop(std::true_type{});
-      else
-        mma_loop(std::false_type{});
-      // drain: every MMA issued above has finished before TMEM is released
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = fwd_unit_index(r);
+        if (u >= n_units) break;
+        const FwdUnit w = fwd_unit<D>(p, u);
+        ok = w.two ? unit_mma(w, std::true_type{}) : unit_mma(w, std::false_type{});
+        ++units;
+        if (w.two) ++units2;
+      }
+      // drain: every MMA issued above has finished before TMEM is released (bounded, and
+      // waited for even after an abort)
       mma_commit(mma_done);
-      mbar_wait(mma_done, 0, abort, p.status);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(mma_done, 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int w = warp >> 2;            // query tile
-    if (w == 1 && !two) goto softmax_done;  // no row of this block falls in query tile 1
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
-    const int row = q0 + w * 128 + r;   // absolute query row
-    const int rpos = p.pos_mod ? row % p.pos_mod : row;  // its position for the causal mask
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + (w ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_off + (w ? C::COL_O1 : C::COL_O0);
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;      // reference max (log2 units) of O and l
-    uint64_t l_exact = 0;          // sum of p (fp32 pair): gives the LSE
-    uint64_t l_round = 0;          // sum of bf16(p), the weights the PV MMA used: normalises O
-    bool ok = true;
-    const int tile_row0 = q0 + w * 128;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    for (int j = 0; j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
+    const int BH = p.B * p.H;
+    int jg = 0;  // key tiles processed by this warpgroup (s_full, o_bar phases)
+    bool ok = true;
+    for (int ru = 0; ok; ++ru) {
+      const int u = fwd_unit_index(ru);
+      if (u >= n_units) break;
+      const FwdUnit wu = fwd_unit<D>(p, u);
+      if (w == 1 && !wu.two) continue;  // no row of this block falls in query tile 1
+      const int row = wu.q0 + w * 128 + r;                 // absolute query row
+      const int rpos = p.pos_mod ? row % p.pos_mod : row;  // its position for the causal mask
+      float m_used = -INFINITY;      // reference max (log2 units) of O and l
+      uint64_t l_exact = 0;          // sum of p (fp32 pair): gives the LSE
+      uint64_t l_round = 0;          // sum of bf16(p), the weights the PV MMA used: normalises O
+      const int tile_row0 = wu.q0 + w * 128;
+      for (int j = 0; j < wu.n_kv; ++j, ++jg) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), jg & 1, ab));
+        if (!ok) break;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tS + 32 * c, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
+        }
+        const int col0 = (wu.j0 + j) * 128;
+        // packed rows: the smallest position in the tile is 0 (+ qoff)
+        if ((p.causal && col0 + 127 > (p.pos_mod ? 0 : tile_row0) + p.qoff) || col0 + 128 > p.Nk) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int col = col0 + c;
+            if ((p.causal && col > rpos + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
+          }
+        }
+        float mx4[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          float m = fmaxf(s[32 * a], s[32 * a + 1]);
+#pragma unroll
+          for (int c = 2; c < 32; c += 2) m = max3f(m, s[32 * a + c], s[32 * a + c + 1]);
+          mx4[a] = m;
+        }
+        const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
+        const float m_tile = mx * sl2;
+        const bool need = m_tile > m_used + p.tau;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? m_tile : m_used;
+          const float alpha = need ? ex2_mufu(m_used - m_new) : 1.f;
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (p.rescale_events) {  // debug counter: rows whose O is rescaled at this key tile
+              const unsigned moved = __ballot_sync(0xffffffffu, alpha != 1.f);
+              if (lane == 0) atomicAdd(p.rescale_events, (unsigned long long)__popc(moved));
+            }
+            // O holds sum_{j'<j} P V against m_used; it must be complete before rescaling
+            ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t rr[16];
+              tmem_ld16(tO + 16 * c, rr);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+              tmem_st16(tO + 16 * c, rr);
+            }
+            tmem_st_wait();
+          }
+          const uint64_t a2 = f2_pack(alpha, alpha);
+          l_exact = f2_mul(l_exact, a2);
+          l_round = f2_mul(l_round, a2);
+          m_used = m_new;
+        }
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        const uint64_t nm2 = f2_pack(neg_m, neg_m);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t x2 = f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nm2);
+            float p0, p1;
+            if ((i * POLY) % 16 < POLY) {
+              const float2 pp = f2_unpack(ex2_poly2(x2));
+              p0 = pp.x;
+              p1 = pp.y;
+            } else {
+              const float2 x = f2_unpack(x2);
+              p0 = ex2_mufu(x.x);
+              p1 = ex2_mufu(x.y);
+            }
+            pk[i] = pack_bf16x2(p0, p1);
+            l_exact = f2_add(l_exact, f2_pack(p0, p1));
+            l_round = f2_add(l_round, bf16x2_widen(pk[i]));
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(w));
+      }
       if (!ok) break;
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tS + 32 * c, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
-      }
-      const int col0 = (j0 + j) * 128;
-      // packed rows: the smallest position in the tile is 0 (+ qoff)
-      if ((p.causal && col0 + 127 > (p.pos_mod ? 0 : tile_row0) + p.qoff) || col0 + 128 > p.Nk) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int col = col0 + c;
-          if ((p.causal && col > rpos + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
-        }
-      }
-      float mx4[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        float m = fmaxf(s[32 * a], s[32 * a + 1]);
-#pragma unroll
-        for (int c = 2; c < 32; c += 2) m = max3f(m, s[32 * a + c], s[32 * a + c + 1]);
-        mx4[a] = m;
-      }
-      const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
-      const float m_tile = mx * sl2;
-      const bool need = m_tile > m_used + p.tau;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? m_tile : m_used;
-        const float alpha = need ? ex2_mufu(m_used - m_new) : 1.f;
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (p.rescale_events) {  // debug counter: rows whose O is rescaled at this key tile
-            const unsigned moved = __ballot_sync(0xffffffffu, alpha != 1.f);
-            if (lane == 0) atomicAdd(p.rescale_events, (unsigned long long)__popc(moved));
-          }
-          // O holds sum_{j'<j} P V against m_used; it must be complete before rescaling
-          ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (j - 1) & 1, abort, p.status));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t rr[16];
-            tmem_ld16(tO + 16 * c, rr);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st16(tO + 16 * c, rr);
-          }
-          tmem_st_wait();
-        }
-        const uint64_t a2 = f2_pack(alpha, alpha);
-        l_exact = f2_mul(l_exact, a2);
-        l_round = f2_mul(l_round, a2);
-        m_used = m_new;
-      }
-      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      const uint64_t nm2 = f2_pack(neg_m, neg_m);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t x2 = f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nm2);
-          float p0, p1;
-          if ((i * POLY) % 16 < POLY) {
-            const float2 pp = f2_unpack(ex2_poly2(x2));
-            p0 = pp.x;
-            p1 = pp.y;
-          } else {
-            const float2 x = f2_unpack(x2);
-            p0 = ex2_mufu(x.x);
-            p1 = ex2_mufu(x.y);
-          }
-          pk[i] = pack_bf16x2(p0, p1);
-          l_exact = f2_add(l_exact, f2_pack(p0, p1));
-          l_round = f2_add(l_round, bf16x2_widen(pk[i]));
-        }
-        tmem_st16(tS + 16 * c, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full(w));
-    }
-    // ---- epilogue: O / l -> bf16, LSE = ln 2 * (m_used + log2 l)
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (n_kv - 1) & 1, abort, p.status));
-    if (ok) {
+      // ---- epilogue: O / l -> bf16, LSE = ln 2 * (m_used + log2 l).  O's tensor memory is
+      // handed back (o_free) right after the last load from it, so the next unit's first PV
+      // MMA can overwrite it while these stores drain.
+      ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
+      if (!ok) break;
       tc_fence_after();
       const float2 le = f2_unpack(l_exact), lr = f2_unpack(l_round);
       const float l = le.x + le.y, lrs = lr.x + lr.y;
       const float inv_l = lrs > 0.f ? 1.f / lrs : 0.f;
       if (p.splits > 1) {  // split-KV partial: fp32 O over this split's keys, LSE in log2 units
-        const size_t prow = ((size_t)sp * BH + bh) * N + row;
+        const size_t prow = ((size_t)wu.sp * BH + wu.bh) * N + row;
         float4* op = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(tO + 32 * c, rr);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(o_free(w));
+          }
           if (row < N) {
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
@@ -382,33 +469,48 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (row < N) p.lse_part[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
       } else {
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * N + row) * D);
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)wu.bh * N + row) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tO + 32 * c, rr);
-        uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tO + 32 * c, rr);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(o_free(w));
+          }
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
-        if (row < N) {
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+          if (row < N) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            orow[c * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 4; ++v4)
+              orow[c * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
-      }
-      if (row < N) p.lse[(size_t)bh * N + row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (row < N) p.lse[(size_t)wu.bh * N + row] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
 
-softmax_done:
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+static int fwd_sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
 }
 
 template <int D, int POLY>
@@ -424,9 +526,11 @@ static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, c
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const long long blocks = (long long)((p.Nq + C::BLOCK - 1) / C::BLOCK) * p.B * p.H * p.splits;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  fwd_kernel<D, POLY><<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  const long long units = (long long)((p.Nq + C::BLOCK - 1) / C::BLOCK) * p.B * p.H * p.splits;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // persistent: one CTA per SM (at most one per unit)
+  const int grid = (int)std::min<long long>(units, fwd_sm_count());
+  fwd_kernel<D, POLY><<<dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p, (int)units);
   return cudaGetLastError();
 }
 

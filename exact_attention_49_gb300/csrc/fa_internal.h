@@ -17,6 +17,7 @@ struct Options {
                                    // releases its deterministic-order counters, 2 = the copy warp skips
                                    // the second query tile's Q/dO load
   int count_rescales = 0;          // count the forward's O rescales into the library's event counter
+  int bwd_2cta = 0;                // backward main stage on CTA pairs (tcgen05 cta_group::2), d = 128
 };
 Options& options();
 
@@ -40,6 +41,8 @@ struct FwdParams {
   float* o_part;     // splits > 1: fp32 [splits][B*H][Nq][d]
   float* lse_part;   // splits > 1: fp32 [splits][B*H][Nq]
   unsigned long long* rescale_events;  // non-null: add the number of rows whose O was rescaled (per key tile)
+  unsigned* kabort;  // kernel-wide abort word (see Abort in sm103.cuh)
+  unsigned gen;      // this launch's generation
 };
 
 struct BwdParams {
@@ -57,6 +60,8 @@ struct BwdParams {
   float scale;        // softmax scale (folded into dS)
   int* status;        // device status word
   int debug_hook;     // failure-injection test hook (Options::debug_bwd_hook)
+  unsigned* kabort;   // kernel-wide abort word (see Abort in sm103.cuh)
+  unsigned gen;       // this launch's generation
 };
 
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
@@ -64,6 +69,10 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* 
                            cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+// The main stage on CTA pairs (d = 128): tq/tdo with 128-row boxes, tq64/tdo64 with 64-row boxes.
+cudaError_t launch_bwd_main_pair(const CUtensorMap& tq, const CUtensorMap& tq64, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdo64,
+                                 const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
 // Merge split-KV partials: LSE = log sum_s 2^lse_s, O = sum_s 2^(lse_s - LSE) o_s (bf16)
 cudaError_t launch_fwd_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse, int splits,
@@ -78,8 +87,9 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 constexpr int kDefaultPolyCols = 0;
 
 // Build a 3-D bf16 tensor map over a contiguous [outer][rows][d] array with a
-// box of 64 x 128 x 1 elements and 128-byte swizzle.  Returns 0 on success.
-int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer);
+// box of 64 x box_rows x 1 elements and 128-byte swizzle.  Returns 0 on success.
+int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long rows, long long outer,
+                        int box_rows = 128);
 
 // Device address of the library's status word on the current device (nullptr on error).
 int* device_status_ptr();
@@ -90,6 +100,11 @@ int bwd_validate(const void* q, const void* k, const void* v, const void* o, con
                  bool* launch);
 // Record `what` and CUDA's error text for fa_last_error_detail; returns FA_ERR_CUDA.
 int report_cuda_error(const char* what, cudaError_t e);
+
+// Device address of the library's kernel-wide abort word on the current device (nullptr on
+// error), and a fresh non-zero generation for the next launch.
+unsigned* abort_word_ptr();
+unsigned next_generation();
 
 // Device address of the library's rescale-event counter on the current device (nullptr on error).
 unsigned long long* rescale_events_ptr();

@@ -49,20 +49,51 @@ FA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase of `bar` with parity `parity` has completed.  Gives up
-// after kWaitLimitNs, or as soon as another thread of the CTA has given up
-// (*abort != 0); a thread that gives up records kStatusTimeout in *status
-// and raises *abort.  Returns false when it gave up.
-FA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+// Where a bounded wait reports that it gave up.  `cta` is the CTA's abort flag (shared
+// memory): once one role of the CTA gives up, the others stop waiting at once.  `grid` is the
+// library's kernel-wide abort word and `gen` this launch's generation (non-zero, different for
+// every launch): a CTA that gives up stores `gen` there, and a wait anywhere in the launch that
+// has lasted over 1 ms and finds it gives up too.  So one systematic failure ends the whole
+// launch after about one wait limit, instead of every later wait running to its own limit;
+// older launches' generations in the word are ignored, so it never needs clearing.
+struct Abort {
+  volatile int* cta;
+  int* status;
+  volatile unsigned* grid;
+  unsigned gen;
+};
+constexpr unsigned long long kGridCheckNs = 1000000ull;  // 1 ms
+
+// Record a failed wait: CTA flag, kernel-wide word, device status (first error wins).
+FA_DEV void give_up(const Abort& ab) {
+  *ab.cta = 1;
+  *ab.grid = ab.gen;
+  atomicCAS(ab.status, 0, kStatusTimeout);
+}
+// True when this CTA or (checked only after `elapsed` ns of waiting) another CTA of the
+// launch has given up.
+FA_DEV bool should_stop(const Abort& ab, unsigned long long elapsed) {
+  if (*ab.cta) return true;
+  if (elapsed > kGridCheckNs && *ab.grid == ab.gen) {
+    *ab.cta = 1;
+    return true;
+  }
+  return false;
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed.  Gives up after
+// kWaitLimitNs, or when should_stop() says so; a thread whose own limit runs out calls
+// give_up().  Returns false when it gave up.
+FA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicCAS(status, 0, kStatusTimeout);
+      const unsigned long long el = globaltimer() - t0;
+      if (should_stop(ab, el)) return false;
+      if (el > kWaitLimitNs) {
+        give_up(ab);
         return false;
       }
     }
@@ -223,6 +254,111 @@ FA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 FA_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// A cluster of two CTAs whose tensor cores work as one: an MMA issued by the even CTA (the
+// leader) computes M = 256 rows (each CTA's tensor memory holds its 128) or M = 128 rows (each
+// CTA holds its 64 rows twice over the 128 lanes: lanes 0-63 carry columns [0, N/2), lanes
+// 64-127 columns [N/2, N), in N/2 tensor-memory columns).  A comes from each CTA's own shared
+// memory or tensor memory (its rows), B is split by columns: each CTA supplies N/2 of them, at
+// the same shared-memory offset in both CTAs.  Every tcgen05 instruction of such a kernel
+// uses cta_group::2.
+FA_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address, in the cluster's shared window, of the same offset in CTA `rank`.
+FA_DEV uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+FA_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier given by its cluster address (this CTA's or the peer's).
+FA_DEV void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// try_wait with cluster-scope acquire: pairs with arrivals released by the peer CTA.
+FA_DEV bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+FA_DEV bool mbar_wait_cl(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      const unsigned long long el = globaltimer() - t0;
+      if (should_stop(ab, el)) return false;
+      if (el > kWaitLimitNs) {
+        give_up(ab);
+        return false;
+      }
+    }
+  }
+}
+// 3-D tiled load into this CTA's shared memory whose completion (tx bytes) is signalled on an
+// mbarrier of either CTA of the pair (`bar_cl`, a cluster address).
+FA_DEV void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cl, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+FA_DEV void st_cluster_v4(uint32_t cl_addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cl_addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+// Generic-proxy writes to this CTA's or the peer's shared memory, made visible to the async
+// proxy (the tensor cores).
+FA_DEV void fence_async_smem_cluster() { asm volatile("fence.proxy.async.shared::cluster;" ::: "memory"); }
+FA_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+FA_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+FA_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+FA_DEV void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+FA_DEV void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` of both CTAs of the pair when every MMA issued
+// so far by this thread has completed.
+FA_DEV void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
 
 // ---------------------------------------------------------------- math helpers
 FA_DEV float ex2_mufu(float x) {

@@ -69,7 +69,8 @@ def test_options_roundtrip(L):
     assert fa.fa_set_option("poly_fraction", 0.3) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_option("poly_fraction", -1) == fa.FA_OK
     assert fa.fa_get_option("poly_exp") == -1
-    for key, good, bad in (("debug_bwd_hook", (0, 1, 2), (3, -1, 0.5)), ("count_rescales", (0, 1), (2, 0.5))):
+    for key, good, bad in (("debug_bwd_hook", (0, 1, 2), (3, -1, 0.5)), ("count_rescales", (0, 1), (2, 0.5)),
+                           ("bwd_2cta", (0, 1), (2, -1))):
         for val in good:
             assert fa.fa_set_option(key, val) == fa.FA_OK
             assert fa.fa_get_option(key) == val

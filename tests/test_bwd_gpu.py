@@ -27,6 +27,17 @@ def _lib():
     fa.lib()
 
 
+@pytest.fixture(autouse=True, params=[0, 1], ids=["1cta", "2cta"])
+def bwd_mode(request):
+    """Every backward test runs on both main-stage kernels: one CTA per 128-key tile, and CTA
+    pairs over 256 keys with tcgen05 cta_group::2 MMAs (head dimension 128; at d = 64 both
+    settings run the one-CTA kernel)."""
+    old = fa.fa_get_option("bwd_2cta")
+    assert fa.fa_set_option("bwd_2cta", request.param) == fa.FA_OK
+    yield request.param
+    fa.fa_set_option("bwd_2cta", old)
+
+
 def gpu_fwd_bwd(q, k, v, do, causal, scale, deterministic=False):
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
@@ -46,7 +57,8 @@ def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0, deterministic=False):
     errs = (rel_fro(to64(dq), rq), rel_fro(to64(dk), rk), rel_fro(to64(dv), rv))
     rows = (row_err(to64(dq), rq), row_err(to64(dk), rk), row_err(to64(dv), rv))
     record("bwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=qk_mult, deterministic=bool(deterministic),
-           dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2], dq_row=rows[0], dk_row=rows[1], dv_row=rows[2])
+           pair=fa.fa_get_option("bwd_2cta"), dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2], dq_row=rows[0],
+           dk_row=rows[1], dv_row=rows[2])
     assert max(errs) <= GRAD_RTOL, errs
     assert max(rows) <= ROW_TOL, rows
     return errs
@@ -94,7 +106,8 @@ def test_bwd_ragged(N, causal, d):
         errs.append(max(rel_fro(g64[b, h], want[b, h]) for b in range(B) for h in range(got.shape[1])))
         rows.append(row_err(g64, want))
     record("bwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=1.0, deterministic=False,
-           dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2], dq_row=rows[0], dk_row=rows[1], dv_row=rows[2])
+           pair=fa.fa_get_option("bwd_2cta"), dq_rel=errs[0], dk_rel=errs[1], dv_rel=errs[2], dq_row=rows[0],
+           dk_row=rows[1], dv_row=rows[2])
     assert max(errs) <= GRAD_RTOL, errs
     assert max(rows) <= ROW_TOL, rows
 
@@ -160,7 +173,8 @@ def test_bwd_full_size_sampled(name, det):
         got = (to64(dq[b:b + 1, hs]), to64(dk[b:b + 1, g:g + 1]), to64(dv[b:b + 1, g:g + 1]))
         errs = tuple(rel_fro(x, r) for x, r in zip(got, (rq, rk, rv)))
         rows = tuple(row_err(x, r) for x, r in zip(got, (rq, rk, rv)))
-        record("bwd_full_size", workload=w.name, deterministic=bool(det), group=[b, g], dq_rel=errs[0],
+        record("bwd_full_size", workload=w.name, deterministic=bool(det), pair=fa.fa_get_option("bwd_2cta"),
+               group=[b, g], dq_rel=errs[0],
                dk_rel=errs[1], dv_rel=errs[2], dq_row=rows[0], dk_row=rows[1], dv_row=rows[2])
         assert max(errs) <= GRAD_RTOL, ((b, g), errs)
         assert max(rows) <= ROW_TOL, ((b, g), rows)
@@ -180,3 +194,20 @@ def test_bwd_deterministic_bit_identical_full_size(name):
     assert fa.fa_last_device_status() == fa.FA_OK
     for a, b in zip(first, again):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_bwd_pair_matches_single_cta():
+    """The two main-stage kernels compute the same sums in a different order (the pair adds
+    each query tile's dQ over 256 keys on chip before the fp32 reductions): their results
+    agree to the rounding of those orders."""
+    B, H, Hkv, N, d = 2, 8, 2, 1000, 128
+    q, k, v, do = (t.cuda() for t in make_inputs(B, H, Hkv, N, d, seed=29))
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    res = []
+    for mode in (0, 1):
+        assert fa.fa_set_option("bwd_2cta", mode) == fa.FA_OK
+        res.append(fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=True))
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for a, b in zip(*res):
+        assert rel_fro(to64(a), to64(b)) < 5e-3

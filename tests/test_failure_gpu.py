@@ -53,14 +53,17 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert max_abs(to64(lse), lse_ref) <= LSE_TOL
 
 
+@pytest.mark.parametrize("pair", [0, 1], ids=["1cta", "2cta"])
 @pytest.mark.parametrize("hook,causal,det", [(1, True, True), (2, False, False)])
-def test_backward_bounded_waits_report_timeout(hook, causal, det):
+def test_backward_bounded_waits_report_timeout(hook, causal, det, pair):
     B, H, Hkv, N, d = 1, 1, 1, 512, 128
     q, k, v, do = make_inputs(B, H, Hkv, N, d, seed=6)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
+    old_pair = fa.fa_get_option("bwd_2cta")
+    assert fa.fa_set_option("bwd_2cta", pair) == fa.FA_OK
     assert fa.fa_set_option("debug_bwd_hook", hook) == fa.FA_OK
     try:
         fa.attention_backward(qd, kd, vd, o, dod, lse, causal=causal, deterministic=det)
@@ -72,6 +75,7 @@ def test_backward_bounded_waits_report_timeout(hook, causal, det):
     dq, dk, dv = fa.attention_backward(qd, kd, vd, o, dod, lse, causal=causal, deterministic=det)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
+    fa.fa_set_option("bwd_2cta", old_pair)
     rq, rk, rv = ref.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, d ** -0.5)
     for got, want in ((dq, rq), (dk, rk), (dv, rv)):
         assert rel_fro(to64(got), want) <= GRAD_RTOL
