@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(384, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (warp == 9 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
-      int it = 0;        // ring position of the next K/V load (continues across units)
-      int issued = 0;    // ring loads issued
+      uint32_t it = 0;      // ring position of the next K/V load (continues across units)
+      uint32_t issued = 0;  // ring loads issued
       int q_loads = 0;   // Q loads issued (one per unit)
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(384, 1)
       if (*abort) {
         // The CTA gave up: let the copies still in flight land before the CTA exits (each
         // completes its slot's phase), bounded at 1 ms per copy.
-        for (int k = max(0, issued - C::STAGES); k < issued; ++k) {
+        for (uint32_t k = issued > C::STAGES ? issued - C::STAGES : 0; k < issued; ++k) {
           const uint64_t t0 = globaltimer();
           while (!mbar_try_wait(full_bar(k % C::STAGES), (k / C::STAGES) & 1) && globaltimer() - t0 < 1000000ull) {
           }
@@ -243,45 +243,48 @@ __global__ void __launch_bounds__(384, 1)
           mma_ts(tmem + (w ? C::COL_O1 : C::COL_O0), tmem + sc + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
                  idO, (acc || kk > 0) ? 1u : 0u);
       };
-      auto slot_of = [&](int k) { return k % C::STAGES; };
-      auto par_of = [&](int k) { return (uint32_t)((k / C::STAGES) & 1); };
-      int it = 0;            // ring position (continues across units)
-      int units = 0;         // units issued (q_full phase, o_free(0) phase)
-      int units2 = 0;        // two-tile units issued (o_free(1) phase)
-      int jg0 = 0, jg1 = 0;  // key tiles issued per query tile (p_full phases)
+      auto slot_of = [](uint32_t k) { return k % C::STAGES; };
+      auto par_of = [](uint32_t k) { return (k / C::STAGES) & 1u; };
+      uint32_t it = 0;          // ring position (continues across units)
+      uint32_t units = 0;       // units issued (q_full phase, o_free(0) phase)
+      uint32_t units2 = 0;      // two-tile units issued (o_free(1) phase)
+      uint32_t jg0 = 0, jg1 = 0;  // key tiles issued per query tile (p_full phases)
       // One unit's MMAs, compiled once for two query tiles and once for one: a run-time branch
-      // on the tile count inside this one-lane issue loop costs about 1% of the kernel.
-      auto unit_mma = [&](const FwdUnit& w, auto two_tiles) -> bool {
+      // on the tile count inside this one-lane issue loop costs about 1% of the kernel.  The
+      // loop reads only values fixed for the unit (ring base, phase bases), so nothing it
+      // needs is written inside it.
+      auto unit_mma = [&](const FwdUnit& w, auto two_tiles, const uint32_t it0, const uint32_t u_idx,
+                          const uint32_t u2_idx, const uint32_t g0, const uint32_t g1) -> bool {
         constexpr bool TWO = decltype(two_tiles)::value;
-        if (!mbar_wait(q_full, units & 1, ab)) return false;
-        if (!mbar_wait(full_bar(slot_of(it)), par_of(it), ab)) return false;
+        const int n_kv = w.n_kv;
+        if (!mbar_wait(q_full, u_idx & 1, ab)) return false;
+        if (!mbar_wait(full_bar(slot_of(it0)), par_of(it0), ab)) return false;
         tc_fence_after();
-        issue_s(0, slot_of(it));
+        issue_s(0, slot_of(it0));
         mma_commit(s_full(0));
         if constexpr (TWO) {
-          issue_s(1, slot_of(it));
+          issue_s(1, slot_of(it0));
           mma_commit(s_full(1));
         }
-        if (w.n_kv == 1) mma_commit(q_empty);  // the unit's last S MMAs: the Q buffer frees after them
-        mma_commit(empty_bar(slot_of(it)));
+        if (n_kv == 1) mma_commit(q_empty);  // the unit's last S MMAs: the Q buffer frees after them
+        mma_commit(empty_bar(slot_of(it0)));
         // The first PV of a query tile overwrites its O accumulator, which the softmax warps
         // of the previous unit may still be reading out; they release it before they start on
         // this unit's first exponentials, so this wait rarely stalls.
-        if (units > 0 && !mbar_wait(o_free(0), (units - 1) & 1, ab)) return false;
+        if (u_idx > 0 && !mbar_wait(o_free(0), (u_idx - 1) & 1, ab)) return false;
         if constexpr (TWO) {
-          if (units2 > 0 && !mbar_wait(o_free(1), (units2 - 1) & 1, ab)) return false;
+          if (u2_idx > 0 && !mbar_wait(o_free(1), (u2_idx - 1) & 1, ab)) return false;
         }
         // one key tile; MORE: another tile follows (the last iteration is peeled so that the
         // test is not a run-time branch of the issue loop)
         auto step = [&](int j, auto more_tiles) -> bool {
           constexpr bool MORE = decltype(more_tiles)::value;
-          const int itv = it + 2 * j + 1, itk = it + 2 * j + 2;
+          const uint32_t itv = it0 + 2 * j + 1, itk = itv + 1;
           if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), ab)) return false;
-          if (!mbar_wait(p_full(0), jg0 & 1, ab)) return false;
+          if (!mbar_wait(p_full(0), (g0 + j) & 1, ab)) return false;
           tc_fence_after();
           issue_pv(0, slot_of(itv), j > 0);
           mma_commit(o_bar(0));
-          ++jg0;
           if constexpr (MORE) {
             if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), ab)) return false;
             tc_fence_after();
@@ -289,11 +292,10 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(s_full(0));
           }
           if constexpr (TWO) {
-            if (!mbar_wait(p_full(1), jg1 & 1, ab)) return false;
+            if (!mbar_wait(p_full(1), (g1 + j) & 1, ab)) return false;
             tc_fence_after();
             issue_pv(1, slot_of(itv), j > 0);
             mma_commit(o_bar(1));
-            ++jg1;
           }
           mma_commit(empty_bar(slot_of(itv)));
           if constexpr (MORE) {
@@ -301,15 +303,14 @@ __global__ void __launch_bounds__(384, 1)
               issue_s(1, slot_of(itk));
               mma_commit(s_full(1));
             }
-            if (j + 2 == w.n_kv) mma_commit(q_empty);
+            if (j + 2 == n_kv) mma_commit(q_empty);
             mma_commit(empty_bar(slot_of(itk)));
           }
           return true;
         };
         bool ok = true;
-        for (int j = 0; ok && j + 1 < w.n_kv; ++j) ok = step(j, std::true_type{});
-        if (ok) ok = step(w.n_kv - 1, std::false_type{});
-        it += 2 * w.n_kv;
+        for (int j = 0; ok && j + 1 < n_kv; ++j) ok = step(j, std::true_type{});
+        if (ok) ok = step(n_kv - 1, std::false_type{});
         return ok;
       };
       bool ok = true;
@@ -317,9 +318,15 @@ __global__ void __launch_bounds__(384, 1)
         const int u = fwd_unit_index(r);
         if (u >= n_units) break;
         const FwdUnit w = fwd_unit<D>(p, u);
-        ok = w.two ? unit_mma(w, std::true_type{}) : unit_mma(w, std::false_type{});
+        ok = w.two ? unit_mma(w, std::true_type{}, it, units, units2, jg0, jg1)
+                   : unit_mma(w, std::false_type{}, it, units, units2, jg0, jg1);
+        it += 2 * w.n_kv;
+        jg0 += w.n_kv;
         ++units;
-        if (w.two) ++units2;
+        if (w.two) {
+          jg1 += w.n_kv;
+          ++units2;
+        }
       }
       // drain: every MMA issued above has finished before TMEM is released (bounded, and
       // waited for even after an abort)
@@ -357,12 +364,11 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc_fence_after();
         float s[128];
+        {
+          uint32_t rr[128];
+          tmem_ld128(tS, rr);  // one load and one wait for the whole row
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tS + 32 * c, rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
+          for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
         }
         const int col0 = (wu.j0 + j) * 128;
         // packed rows: the smallest position in the tile is 0 (+ qoff)
