@@ -357,7 +357,11 @@ __global__ void __launch_bounds__(384, 1)
       const int rpos = p.pos_mod ? row % p.pos_mod : row;  // its position for the causal mask
       float m_used = -INFINITY;      // reference max (log2 units) of O and l
       uint64_t l_exact = 0;          // sum of p (fp32 pair): gives the LSE
-      uint64_t l_round = 0;          // sum of bf16(p), the weights the PV MMA used: normalises O
+      // sum of bf16(p), the weights the PV MMA used: normalises O.  Two accumulators, each
+      // taking both halves of every other packed pair through mixed-precision adds (fewer
+      // instructions and shorter dependency chains than widening the pairs: 0.900 -> 0.864 ms
+      // on the B4 H16 N8192 causal workload)
+      float lr0 = 0.f, lr1 = 0.f;
       const int tile_row0 = wu.q0 + w * 128;
       for (int j = 0; j < wu.n_kv; ++j, ++jg) {
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), jg & 1, ab));
@@ -414,7 +418,8 @@ __global__ void __launch_bounds__(384, 1)
           }
           const uint64_t a2 = f2_pack(alpha, alpha);
           l_exact = f2_mul(l_exact, a2);
-          l_round = f2_mul(l_round, a2);
+          lr0 *= alpha;
+          lr1 *= alpha;
           m_used = m_new;
         }
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
@@ -437,7 +442,10 @@ __global__ void __launch_bounds__(384, 1)
             }
             pk[i] = pack_bf16x2(p0, p1);
             l_exact = f2_add(l_exact, f2_pack(p0, p1));
-            l_round = f2_add(l_round, bf16x2_widen(pk[i]));
+            if (i & 1)
+              lr1 = add_bf16_hi(add_bf16_lo(lr1, pk[i]), pk[i]);
+            else
+              lr0 = add_bf16_hi(add_bf16_lo(lr0, pk[i]), pk[i]);
           }
           tmem_st16(tS + 16 * c, pk);
         }
@@ -452,8 +460,8 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
       if (!ok) break;
       tc_fence_after();
-      const float2 le = f2_unpack(l_exact), lr = f2_unpack(l_round);
-      const float l = le.x + le.y, lrs = lr.x + lr.y;
+      const float2 le = f2_unpack(l_exact);
+      const float l = le.x + le.y, lrs = lr0 + lr1;
       const float inv_l = lrs > 0.f ? 1.f / lrs : 0.f;
       if (p.splits > 1) {  // split-KV partial: fp32 O over this split's keys, LSE in log2 units
         const size_t prow = ((size_t)wu.sp * BH + wu.bh) * N + row;

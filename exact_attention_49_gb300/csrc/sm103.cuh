@@ -397,6 +397,15 @@ FA_DEV float max3f(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// acc + (the low / high bf16 half of a packed pair, exactly as fp32): one mixed-precision add.
+FA_DEV float add_bf16_lo(float acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t}" : "+f"(acc) : "r"(pk));
+  return acc;
+}
+FA_DEV float add_bf16_hi(float acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}" : "+f"(acc) : "r"(pk));
+  return acc;
+}
 // The two bf16 values of a packed pair, widened exactly to fp32 (as a packed pair).
 FA_DEV uint64_t bf16x2_widen(uint32_t pk) { return f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)); }
 
