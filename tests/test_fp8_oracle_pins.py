@@ -205,3 +205,97 @@ def test_fp8_incoherent_processing_gain_on_outlier_channels(mag):
             err[mode] = (float(np.sqrt(np.mean((o - o_ref) ** 2))), float(np.mean(np.abs(lse - lse_ref))))
         assert err["tensor"][0] >= 2.0 * err["block_incoherent"][0], err
         assert err["tensor"][1] >= 1.5 * err["block_incoherent"][1], err
+
+
+# ---------------------------------------------------------------- the FP8 kernel's steps
+
+def test_fwht_fp32_equals_the_sylvester_matrix_exactly_on_integers():
+    # integer inputs keep every fp32 sum exact, so the butterfly must equal x @ H bit for bit
+    rng = np.random.default_rng(4)
+    x = rng.integers(-8, 9, size=(5, 128)).astype(np.float64)
+    h = np.array([[1.0]])
+    while h.shape[0] < 128:
+        h = np.block([[h, h], [h, -h]])
+    np.testing.assert_array_equal(fp8.fwht_fp32(x).astype(np.float64), x @ h)
+
+
+def test_rotate_fp32_is_the_hadamard_rotation_to_fp32_precision():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((4, 128))
+    m = fp8.hadamard_rotation(128, seed=9)
+    signs = np.sign(m[0])  # the first row of H is all ones, so row 0 of M is r / sqrt(d)
+    got = fp8.rotate_fp32(x.astype(np.float32), signs).astype(np.float64)
+    np.testing.assert_allclose(got, x.astype(np.float32).astype(np.float64) @ m, rtol=0, atol=2e-6)
+
+
+def test_e4m3_bytes_match_torch_bit_patterns():
+    vals = fp8.e4m3_values()
+    allv = np.concatenate([vals, -vals[1:]])
+    t = torch.from_numpy(allv.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(fp8.e4m3_bytes(allv), t)
+
+
+def test_quantize_fp32_hand_values():
+    # one block, amax 4: inv = 448 / 4 = 112 and scale = 4 / 448 exactly in fp32;
+    # 3 * 112 = 336 -> tie between 320 and 352 (spacing 32 in [256, 512)) -> 320 (even)
+    x = np.array([[4.0], [3.0], [1.0], [0.01]], dtype=np.float32)[None, None]
+    codes, sc = fp8.quantize_fp32(x)
+    np.testing.assert_array_equal(codes[0, 0, :, 0], [448.0, 320.0, 112.0, fp8.e4m3_round(np.float32(0.01) * np.float32(112))])
+    assert sc[0, 0, 0] == np.float32(4.0) / np.float32(448.0)
+
+
+def test_quantize_fp32_agrees_with_the_fp64_quantiser():
+    # same method, the code decided in fp32 instead of fp64: equal except where the scaled value
+    # lies within fp32 rounding of an e4m3 rounding boundary
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((2, 3, 300, 64)) * np.exp(rng.uniform(-3, 3, (2, 3, 300, 1)))).astype(np.float32)
+    codes, sc = fp8.quantize_fp32(x)
+    x64 = x.astype(np.float64)
+    codes64 = np.empty_like(x64)
+    for ib in range(3):
+        blk = x64[..., 128 * ib:128 * (ib + 1), :]
+        s64 = np.max(np.abs(blk), axis=(-2, -1), keepdims=True) / 448.0
+        codes64[..., 128 * ib:128 * (ib + 1), :] = fp8.e4m3_round(blk / s64)
+        np.testing.assert_allclose(sc[..., ib], s64[..., 0, 0], rtol=2 ** -23, atol=0)
+    differ = np.mean(codes != codes64)
+    assert differ < 1e-3, differ
+    np.testing.assert_allclose(codes, codes64, rtol=2 ** -3, atol=0)
+
+
+def _quantised_inputs(seed, B=1, H=2, Hkv=1, N=300, d=64):
+    rng = np.random.default_rng(seed)
+    q, k, v = rng.standard_normal((B, H, N, d)), rng.standard_normal((B, Hkv, N, d)), rng.standard_normal((B, Hkv, N, d))
+    v[..., 200:, :] *= 5.0  # a different V scale in the last blocks
+    (q8, sq), (k8, sk), (v8, sv) = (fp8.quantize_fp32(t) for t in (q, k, v))
+    return q8, sq, k8, sk, v8, sv
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiled_fp8_attention_without_p_rounding_is_exact_attention(causal):
+    q8, sq, k8, sk, v8, sv = _quantised_inputs(7)
+    o, lse = fp8.fp8_attention_tiled(q8, k8, v8, sq, sk, sv, causal, 0.125, quantize_p=False)
+    deq = lambda c, s: c * np.repeat(s.astype(np.float64), 128, axis=-1)[..., :c.shape[-2], None]
+    o_ref, lse_ref = ref.attn_fwd(deq(q8, sq), deq(k8, sk), deq(v8, sv), causal, 0.125)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_tiled_fp8_attention_constant_v_is_returned_exactly():
+    q8, sq, k8, sk, _, _ = _quantised_inputs(8)
+    v8 = np.full(k8.shape, 112.0)
+    sv = np.full(sk.shape, 1.0 / 112, dtype=np.float32)
+    o, _ = fp8.fp8_attention_tiled(q8, k8, v8, sq, sk, sv, True, 0.125)
+    np.testing.assert_allclose(o, 112.0 * np.float64(np.float32(1.0 / 112)), rtol=1e-14, atol=0)
+
+
+def test_tiled_fp8_attention_hand_case():
+    # one query, three keys in one tile, scores (0, 0, ln 3) from unit codes and scale ln 3;
+    # weights exp(s - max) = (1/3, 1/3, 1); 448 * (1/3) = 149.3 in [128, 256), spacing 16:
+    # 9.33 -> 9 -> 144; 448 stays.  O = (144 * 1 + 144 * 2 + 448 * 4) / (144 + 144 + 448)
+    q8 = np.array([[[[1.0, 0.0]]]])
+    k8 = np.array([[[[0.0, 1.0], [0.0, 1.0], [1.0, 0.0]]]])
+    v8 = np.array([[[[1.0, 0.0], [2.0, 0.0], [4.0, 0.0]]]])
+    one = np.ones((1, 1, 1), dtype=np.float32)
+    o, lse = fp8.fp8_attention_tiled(q8, k8, v8, one, one, one, False, float(np.log(3.0)))
+    assert o[0, 0, 0, 0] == pytest.approx(2224.0 / 736.0, rel=1e-14)
+    assert lse[0, 0, 0] == pytest.approx(np.log(5.0), rel=1e-14)
