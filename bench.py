@@ -271,6 +271,8 @@ def run_ours(args, w):
         raise SystemExit("bad --poly-exp %r" % args.poly_exp)
     if args.bwd_2cta is not None and fa.fa_set_option("bwd_2cta", args.bwd_2cta) != fa.FA_OK:
         raise SystemExit("bad --bwd-2cta %r" % args.bwd_2cta)
+    if args.fwd_2cta is not None and fa.fa_set_option("fwd_2cta", args.fwd_2cta) != fa.FA_OK:
+        raise SystemExit("bad --fwd-2cta %r" % args.fwd_2cta)
     ws_bytes = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d, det)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -408,6 +410,7 @@ def run_ours(args, w):
         "gpu_launches": (1 if fwd_only else 4) * args.steps,
         "poly_exp": fa.fa_get_option("poly_exp"),
         "bwd_2cta": fa.fa_get_option("bwd_2cta"),
+        "fwd_2cta": fa.fa_get_option("fwd_2cta"),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -499,6 +502,71 @@ def run_decode(args):
     return 0
 
 
+def run_fp8(args, w):
+    """Time the FP8 forward (fa_fwd_fp8, d = 128) on a workload, with the quantisation
+    (fa_fp8_quantize, incoherent processing on) timed separately.  Throughput is the forward FLOP
+    count over the attention kernel's time, against the dense FP8 peak taken as twice the
+    measured bf16 peak (the nominal fp8 / bf16 ratio)."""
+    import torch
+    from exact_attention_49_gb300 import binding as fa
+    from exact_attention_49_gb300.inputs import workload_inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q, k, v, _ = (t.to(dev) for t in workload_inputs(w))
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    signs = torch.tensor([1.0 if (i * 2654435761) % 7 < 4 else -1.0 for i in range(d)], dtype=torch.float32,
+                         device=dev)
+    need = fa.fa_fp8_workspace_bytes(B, H, Hkv, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def quant():
+        st = fa.fa_fp8_quantize(q, k, v, signs, B, H, Hkv, N, d, ws, need, stream)
+        if st != fa.FA_OK:
+            raise fa.FAError("fa_fp8_quantize", st)
+
+    def attn():
+        st = fa.fa_fwd_fp8(ws, need, o, lse, B, H, Hkv, N, d, int(w.causal), w.scale, stream)
+        if st != fa.FA_OK:
+            raise fa.FAError("fa_fwd_fp8", st)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_q = timed(quant, max(3, args.steps // 4))
+    with ClockSampler(0) as clk:
+        ms = timed(attn, args.steps)
+    clocks = clk.summary()
+    st = fa.fa_last_device_status(stream)
+    if st != fa.FA_OK:
+        raise fa.FAError("device status", st)
+    f = flops_fwd(B, H, N, d, w.causal)
+    peaks, src = measured_peaks()
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    tf = f / (ms * 1e-3) / 1e12
+    line = {"metric": "FP8 attention forward TFLOP/s (e4m3, 1×GB300)", "value": tf, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": config_of(w, fwd_only=True), "quantize_ms": ms_q,
+            "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "peak_source": "2 x %s bf16_tflops (nominal fp8/bf16 ratio)" % src},
+            "frac_of_nominal_4500": tf / 4500.0, "gpu_launches": args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,6 +586,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--bwd-2cta", type=int, default=None, choices=[0, 1],
                     help="backward main stage on CTA pairs (1) or one CTA per key tile (0); default: library's")
+    ap.add_argument("--fp8", action="store_true", help="time the FP8 forward (d = 128) instead")
+    ap.add_argument("--fwd-2cta", type=int, default=None, choices=[0, 1],
+                    help="forward on CTA pairs with P in shared memory (1) or one CTA per block (0); default: library's")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -533,6 +604,8 @@ def main():
         w = dataclasses.replace(w, B=args.batch, name=w.name.replace("B%d " % w.B, "B%d " % args.batch))
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.fp8:
+        return run_fp8(args, w)
     return run_ours(args, w)
 
 

@@ -46,6 +46,10 @@ _SIGNATURES = {
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
     "fa_bwd_main": (_I, [_P] * 7 + [_I] * 6 + [_F, _I, _P, _S, _P]),
     "fa_bwd_postprocess": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_fp8_workspace_bytes": (_S, [_I] * 5),
+    "fa_fp8_workspace_layout": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_fp8_quantize": (_I, [_P] * 4 + [_I] * 5 + [_P, _S, _P]),
+    "fa_fwd_fp8": (_I, [_P, _S, _P, _P] + [_I] * 6 + [_F, _P]),
     "fa_set_option": (_I, [ctypes.c_char_p, ctypes.c_double]),
     "fa_get_option": (_I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double)]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -164,6 +168,29 @@ def fa_bwd_postprocess(dq, B, H, Hkv, N, d, deterministic, workspace, workspace_
                                     _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def fa_fp8_workspace_bytes(B, H, Hkv, N, d) -> int:
+    return int(lib().fa_fp8_workspace_bytes(B, H, Hkv, N, d))
+
+
+def fa_fp8_workspace_layout(B, H, Hkv, N, d):
+    """Byte offsets (q8, k8, v8t, sq, sk, sv, vmax, total) of the FP8 workspace."""
+    out = (ctypes.c_size_t * 8)()
+    st = lib().fa_fp8_workspace_layout(B, H, Hkv, N, d, out)
+    if st != FA_OK:
+        raise FAError("fa_fp8_workspace_layout", st)
+    return [int(x) for x in out]
+
+
+def fa_fp8_quantize(q, k, v, signs, B, H, Hkv, N, d, workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), _ptr(signs), B, H, Hkv, N, d, _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_fp8(workspace, workspace_bytes, o, lse, B, H, Hkv, N, d, causal, scale, stream=None) -> int:
+    return lib().fa_fwd_fp8(_ptr(workspace), int(workspace_bytes), _ptr(o), _ptr(lse), B, H, Hkv, N, d, int(causal),
+                            float(scale), _stream(stream))
+
+
 def fa_set_option(key: str, value: float) -> int:
     return lib().fa_set_option(key.encode(), float(value))
 
@@ -266,3 +293,28 @@ def attention_backward(q, k, v, o, do, lse, causal: bool = False, scale: float |
         _check("fa_bwd_qk", fa_bwd_qk(q, k, v, o, do, lse, dq, dk, dv, B, H, Hkv, N, Nk, d, causal, scale,
                                       deterministic, workspace, workspace.numel(), stream))
     return dq, dk, dv
+
+
+def attention_forward_fp8(q, k, v, causal: bool = False, scale: float | None = None, signs=None, out=None, lse=None,
+                          workspace=None, stream=None):
+    """FP8 forward (d = 128): quantise q, k, v (rotating q and k by the signed Hadamard matrix
+    when ``signs`` is given: a CUDA float tensor of 128 values +-1) and run attention on the
+    codes.  Returns (o bf16, lse fp32, workspace)."""
+    import torch
+    B, H, Hkv, N, Nk, d = _dims(q, k)
+    if Nk != N:
+        raise ValueError("the FP8 forward takes equal query and key lengths")
+    if scale is None:
+        scale = d ** -0.5
+    need = fa_fp8_workspace_bytes(B, H, Hkv, N, d)
+    if need == 0:
+        raise FAError("fa_fp8_workspace_bytes", FA_ERR_UNSUPPORTED)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("fa_fp8_quantize", fa_fp8_quantize(q, k, v, signs, B, H, Hkv, N, d, workspace, workspace.numel(), stream))
+    _check("fa_fwd_fp8", fa_fwd_fp8(workspace, workspace.numel(), out, lse, B, H, Hkv, N, d, causal, scale, stream))
+    return out, lse, workspace

@@ -79,7 +79,7 @@ FWD_LAUNCH_REGISTERS = 168
 
 def check_register_split(report: dict) -> None:
     for name, r in report.items():
-        if "fwd_kernel" in name and r["registers"] != FWD_LAUNCH_REGISTERS:
+        if ("fwd_kernel" in name or "fwd_pair_kernel" in name) and r["registers"] != FWD_LAUNCH_REGISTERS:
             raise RuntimeError("%s compiled at %s registers per thread, not %d: the setmaxnreg split of the "
                                "forward kernel would not add up" % (name, r["registers"], FWD_LAUNCH_REGISTERS))
 

@@ -132,6 +132,24 @@ int make_tmap_bf16_rows(CUtensorMap* map, const void* base, int d, long long row
   return 0;
 }
 
+int make_tmap_u8(CUtensorMap* map, const void* base, long long inner, long long pitch, long long rows,
+                 long long outer) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)pitch, (cuuint64_t)(pitch * rows)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_detail, sizeof(g_detail), "cuTensorMapEncodeTiled (uint8): CUresult %d", (int)r);
+    return -1;
+  }
+  return 0;
+}
+
 // sm_103 check, cached per device.
 static int check_device() {
   static int state[64] = {};  // 0 unknown, 1 ok, 2 unsupported
@@ -235,6 +253,11 @@ int fa_set_option(const char* key, double value) {
     options().bwd_2cta = static_cast<int>(value);
     return FA_OK;
   }
+  if (!std::strcmp(key, "fwd_2cta")) {
+    if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+    options().fwd_2cta = static_cast<int>(value);
+    return FA_OK;
+  }
   if (!std::strcmp(key, "rescale_events")) {  // only 0: clear the counter (synchronises the device)
     if (value != 0.0) return FA_ERR_INVALID_ARG;
     unsigned long long* p = rescale_events_ptr();
@@ -259,6 +282,7 @@ int fa_get_option(const char* key, double* value) {
   if (!std::strcmp(key, "debug_bwd_hook")) { *value = options().debug_bwd_hook; return FA_OK; }
   if (!std::strcmp(key, "count_rescales")) { *value = options().count_rescales; return FA_OK; }
   if (!std::strcmp(key, "bwd_2cta")) { *value = options().bwd_2cta; return FA_OK; }
+  if (!std::strcmp(key, "fwd_2cta")) { *value = options().fwd_2cta; return FA_OK; }
   if (!std::strcmp(key, "rescale_events")) {  // synchronises the device, then reads the counter
     unsigned long long* p = rescale_events_ptr();
     if (!p) return FA_ERR_CUDA;
@@ -330,7 +354,14 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.gen = next_generation();
   // the exponential-split ablation is built for d = 64 and 128 only
   const int poly = (d == 256 || options().poly_exp < 0) ? kDefaultPolyCols : options().poly_exp;
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (d == 128 && poly == 0 && options().fwd_2cta) {  // CTA pairs (MUFU exponentials)
+    CUtensorMap tk64;
+    if (make_tmap_bf16_rows(&tk64, k, d, Nk, (long long)B * Hkv, 64)) return FA_ERR_CUDA;
+    e = launch_fwd_pair(tq, tk64, tv, p, static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_fwd(d, tq, tk, tv, p, poly, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd launch", e);
 }
 
@@ -643,6 +674,117 @@ int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o, const 
   st = bwd_main_impl(q, k, v, dout, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale, deterministic, workspace, stream);
   if (st) return st;
   return bwd_post_impl(dq, B, H, Nq, d, workspace, stream);
+}
+
+// FP8 workspace layout (each part 256-byte aligned), nb = ceil(N / 128), Np = N rounded up to
+// 16: q8 [B*H][N][128], k8 [B*Hkv][N][128], v8t [B*Hkv][128][Np] (e4m3 codes), then fp32 sq
+// [B*H][nb], sk [B*Hkv][nb], sv [B*Hkv][nb], vmax [B*Hkv].
+static int fp8_layout(int B, int H, int Hkv, int N, size_t off[8]) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t nb = (size_t)(N + 127) / 128, Np = ((size_t)N + 15) / 16 * 16;
+  off[0] = 0;
+  off[1] = up(off[0] + (size_t)B * H * N * 128);
+  off[2] = up(off[1] + (size_t)B * Hkv * N * 128);
+  off[3] = up(off[2] + (size_t)B * Hkv * 128 * Np);
+  off[4] = up(off[3] + (size_t)B * H * nb * 4);
+  off[5] = up(off[4] + (size_t)B * Hkv * nb * 4);
+  off[6] = up(off[5] + (size_t)B * Hkv * nb * 4);
+  off[7] = up(off[6] + (size_t)B * Hkv * 4);  // total
+  return 0;
+}
+
+static int check_fp8_shape(int B, int H, int Hkv, int N, int d) {
+  int st = check_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (d != 128) return fail_detail(FA_ERR_UNSUPPORTED, "the FP8 forward supports d = 128");
+  return FA_OK;
+}
+
+size_t fa_fp8_workspace_bytes(int B, int H, int Hkv, int N, int d) {
+  if (check_fp8_shape(B, H, Hkv, N, d)) return 0;
+  size_t off[8];
+  fp8_layout(B, H, Hkv, N, off);
+  return off[7];
+}
+
+int fa_fp8_workspace_layout(int B, int H, int Hkv, int N, int d, size_t* offsets) {
+  int st = check_fp8_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (!offsets) return FA_ERR_INVALID_ARG;
+  fp8_layout(B, H, Hkv, N, offsets);
+  return FA_OK;
+}
+
+int fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs, int B, int H, int Hkv, int N,
+                    int d, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_fp8_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (B == 0 || N == 0) return FA_OK;
+  size_t off[8];
+  fp8_layout(B, H, Hkv, N, off);
+  if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < off[7]) return FA_ERR_WORKSPACE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(signs, 4) || !aligned(workspace, 256))
+    return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float c = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  const int Np = (N + 15) / 16 * 16;
+  const bool rot = signs != nullptr;
+  cudaError_t e = launch_fp8_quantize(q, ws + off[0], reinterpret_cast<float*>(ws + off[3]), signs, c,
+                                      (long long)B * H, N, rot, false, 0, s);
+  if (e == cudaSuccess)
+    e = launch_fp8_quantize(k, ws + off[1], reinterpret_cast<float*>(ws + off[4]), signs, c, (long long)B * Hkv, N,
+                            rot, false, 0, s);
+  if (e == cudaSuccess)
+    e = launch_fp8_quantize(v, ws + off[2], reinterpret_cast<float*>(ws + off[5]), nullptr, c, (long long)B * Hkv, N,
+                            false, true, Np, s);
+  if (e == cudaSuccess)
+    e = launch_fp8_vmax(reinterpret_cast<const float*>(ws + off[5]), reinterpret_cast<float*>(ws + off[6]),
+                        (long long)B * Hkv, N, s);
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_fp8_quantize launch", e);
+}
+
+int fa_fwd_fp8(const void* workspace, size_t workspace_bytes, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+               int causal, float scale, void* stream) {
+  int st = check_fp8_shape(B, H, Hkv, N, d);
+  if (st) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale))) return st;
+  if (B == 0 || N == 0) return FA_OK;
+  size_t off[8];
+  fp8_layout(B, H, Hkv, N, off);
+  if (!o || !lse) return FA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < off[7]) return FA_ERR_WORKSPACE;
+  if (!aligned(o, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const int Np = (N + 15) / 16 * 16;
+  CUtensorMap tq, tk, tvt;
+  if (make_tmap_u8(&tq, ws + off[0], 128, 128, N, (long long)B * H) ||
+      make_tmap_u8(&tk, ws + off[1], 128, 128, N, (long long)B * Hkv) ||
+      make_tmap_u8(&tvt, ws + off[2], Np, Np, 128, (long long)B * Hkv))
+    return FA_ERR_CUDA;
+  Fp8Params p{};
+  p.o = o;
+  p.lse = lse;
+  p.sq = reinterpret_cast<const float*>(ws + off[3]);
+  p.sk = reinterpret_cast<const float*>(ws + off[4]);
+  p.sv = reinterpret_cast<const float*>(ws + off[5]);
+  p.vmax = reinterpret_cast<const float*>(ws + off[6]);
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  if (!(p.kabort = abort_word_ptr())) return FA_ERR_CUDA;
+  p.gen = next_generation();
+  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("fa_fwd_fp8 launch", e);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,

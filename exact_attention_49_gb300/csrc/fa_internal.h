@@ -18,6 +18,7 @@ struct Options {
                                    // the second query tile's Q/dO load
   int count_rescales = 0;          // count the forward's O rescales into the library's event counter
   int bwd_2cta = 0;                // backward main stage on CTA pairs (tcgen05 cta_group::2), d = 128
+  int fwd_2cta = 0;                // forward on CTA pairs with P in shared memory, d = 128
 };
 Options& options();
 
@@ -64,6 +65,34 @@ struct BwdParams {
   unsigned gen;       // this launch's generation
 };
 
+// FP8 forward (fa_fp8.cu), head dimension 128.
+struct Fp8Params {
+  void* o;              // bf16 [B,H,N,128]
+  float* lse;           // fp32 [B,H,N], natural log
+  const float* sq;      // block scales [B*H][nb], [B*Hkv][nb] (nb = ceil(N / 128))
+  const float* sk;
+  const float* sv;
+  const float* vmax;    // largest V block scale per K/V head [B*Hkv]
+  int B, H, Hkv, N;
+  int causal;
+  float scale_log2;     // softmax scale * log2(e)
+  int* status;
+  unsigned* kabort;
+  unsigned gen;
+};
+// Quantise one tensor [heads][N][128] (bf16) to e4m3 codes with one scale per 128-row block;
+// rotate: incoherent processing with signs (d floats, +-1, device memory) and 1/sqrt(d);
+// transpose: write codes as [heads][128][pitch] (V).
+cudaError_t launch_fp8_quantize(const void* x, void* out, float* scales, const float* signs, float inv_sqrt_d,
+                                long long heads, int N, bool rotate, bool transpose, int pitch, cudaStream_t stream);
+cudaError_t launch_fp8_vmax(const float* sv, float* vmax, long long heads, int N, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const Fp8Params& p,
+                           cudaStream_t stream);
+// 3-D uint8 tensor map over [outer][rows][inner] bytes (row pitch `pitch` bytes) with a
+// 128 x 128 byte box and 128-byte swizzle.  Returns 0 on success.
+int make_tmap_u8(CUtensorMap* map, const void* base, long long inner, long long pitch, long long rows,
+                 long long outer);
+
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
                            float* dq_acc, int* counters, long long heads, int N, long long n_counters,
                            cudaStream_t stream);
@@ -74,6 +103,10 @@ cudaError_t launch_bwd_main_pair(const CUtensorMap& tq, const CUtensorMap& tq64,
                                  const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdo64,
                                  const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
+// The forward on CTA pairs (d = 128, one split, MUFU exponentials): tq and tv with 128-row
+// boxes, tk64 with a 64-row box.
+cudaError_t launch_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk64, const CUtensorMap& tv, const FwdParams& p,
+                            cudaStream_t stream);
 // Merge split-KV partials: LSE = log sum_s 2^lse_s, O = sum_s 2^(lse_s - LSE) o_s (bf16)
 cudaError_t launch_fwd_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse, int splits,
                                long long rows, cudaStream_t stream);

@@ -149,6 +149,38 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
 int fa_bwd_postprocess(void* dq, int B, int H, int Hkv, int N, int d,
                        int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
+/* FP8 (e4m3) forward, head dimension 128: block quantisation with incoherent
+ * processing ("FlashAttention" wiki note, section FA3 item 3).  Two calls:
+ *
+ * fa_fp8_quantize writes the quantised inputs into a caller workspace of
+ * fa_fp8_workspace_bytes(...) bytes (256-byte aligned).  q [B,H,N,128], k, v
+ * [B,Hkv,N,128] bf16.  If `signs` (device memory, 128 floats, each +1 or -1)
+ * is not NULL, every row of Q and K is first rotated by H diag(signs)/sqrt(128),
+ * H the Sylvester Hadamard matrix (a fast Walsh-Hadamard transform in fp32),
+ * which leaves Q K^T unchanged; the random signs are the caller's.  Each block
+ * of 128 rows of one head gets one scale, amax / 448, and the codes
+ * e4m3(x * 448 / amax) (round to nearest even, saturating).  Workspace layout
+ * (byte offsets from fa_fp8_workspace_layout, 8 values, the last the total):
+ * q8 [B*H][N][128], k8 [B*Hkv][N][128], v8 transposed [B*Hkv][128][Np] (Np = N
+ * rounded up to 16, padding zero), then fp32 block scales sq [B*H][nb],
+ * sk [B*Hkv][nb], sv [B*Hkv][nb] (nb = ceil(N/128)) and vmax [B*Hkv] (the
+ * largest V block scale of each K/V head).
+ *
+ * fa_fwd_fp8 computes attention from that workspace: S from the codes with
+ * fp32 accumulation and the block scales, an exact running max, the weights
+ * quantised to e4m3 (448 * (sv_block / vmax) * p, the V block scale folded in),
+ * O normalised by the sum of the quantised weights, LSE from the unquantised
+ * sum.  Outputs o bf16 [B,H,N,128], lse fp32 [B,H,N] (natural log); causal masks
+ * are top-left aligned.  The pages give no formats, block sizes or matrices:
+ * these are this library's readings (e4m3, 128-row blocks, amax/448 scales). */
+size_t fa_fp8_workspace_bytes(int B, int H, int Hkv, int N, int d);
+int fa_fp8_workspace_layout(int B, int H, int Hkv, int N, int d, size_t* offsets);
+int fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs,
+                    int B, int H, int Hkv, int N, int d, void* workspace, size_t workspace_bytes,
+                    void* stream);
+int fa_fwd_fp8(const void* workspace, size_t workspace_bytes, void* o, float* lse,
+               int B, int H, int Hkv, int N, int d, int causal, float scale, void* stream);
+
 /* Size of the scratch array that fa_bwd_noalloc uses (32 MiB per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -199,6 +231,14 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *   "rescale_events"     the counter: fa_get_option synchronises the device and
  *                        reads it; fa_set_option(.., 0) synchronises and clears
  *                        it (any other value is rejected).
+ *   "bwd_2cta"           1: the backward's main stage runs on CTA pairs (tcgen05
+ *                        cta_group::2 MMAs over 256 keys, dS exchanged through
+ *                        distributed shared memory), d = 128; 0 (default): one
+ *                        CTA per 128-key tile (FA4's two-CTA backward mode, the
+ *                        ai-papers.net summary, 提案手法 item 3).
+ *   "fwd_2cta"           1: the forward runs on CTA pairs (M = 256 MMAs over 512
+ *                        query rows, P in shared memory), d = 128, one split,
+ *                        MUFU exponentials; 0: one CTA per 256 query rows.
  *   "debug_drop_kv_load" failure-injection test hook, 0 (default) or 1: the
  *                        forward's copy warp skips its second K/V tile load, so
  *                        the MMA warp's bounded wait gives up (after ~2 s), the

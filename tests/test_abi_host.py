@@ -70,7 +70,7 @@ def test_options_roundtrip(L):
     assert fa.fa_set_option("poly_fraction", -1) == fa.FA_OK
     assert fa.fa_get_option("poly_exp") == -1
     for key, good, bad in (("debug_bwd_hook", (0, 1, 2), (3, -1, 0.5)), ("count_rescales", (0, 1), (2, 0.5)),
-                           ("bwd_2cta", (0, 1), (2, -1))):
+                           ("bwd_2cta", (0, 1), (2, -1)), ("fwd_2cta", (0, 1), (2, -1))):
         for val in good:
             assert fa.fa_set_option(key, val) == fa.FA_OK
             assert fa.fa_get_option(key) == val
@@ -273,3 +273,39 @@ def test_noalloc_validates_like_fa_bwd(L):
         assert want != 0 and got == want, (c, got, want)
     # nothing to do: both return FA_OK without touching the GPU
     assert L.fa_bwd_noalloc(*([GOOD] * 9), 0, 2, 1, 128, 64, 0, 0.125, 0, None) == 0
+
+
+def test_fp8_validation(L):
+    """FP8 entry points: sizes, head dimension, arguments and workspace checks, all before any
+    GPU call."""
+    from exact_attention_49_gb300 import binding as fa
+    need = fa.fa_fp8_workspace_bytes(2, 4, 2, 300, 128)
+    off = fa.fa_fp8_workspace_layout(2, 4, 2, 300, 128)
+    nb, Np = 3, 304
+    assert off[1] >= 2 * 4 * 300 * 128 and off[2] - off[1] >= 2 * 2 * 300 * 128
+    assert off[3] - off[2] >= 2 * 2 * 128 * Np and off[4] - off[3] >= 2 * 4 * nb * 4
+    assert all(o % 256 == 0 for o in off) and off[7] == need
+    assert fa.fa_fp8_workspace_bytes(2, 4, 2, 300, 64) == 0
+    assert fa.fa_fp8_workspace_bytes(2, 4, 3, 300, 128) == 0
+    P_ = ctypes.c_void_p
+    L.fa_fwd_fp8.argtypes = [P_, ctypes.c_size_t, P_, P_] + [ctypes.c_int] * 6 + [ctypes.c_float, P_]
+    L.fa_fwd_fp8.restype = ctypes.c_int
+    L.fa_fp8_quantize.argtypes = [P_] * 4 + [ctypes.c_int] * 5 + [P_, ctypes.c_size_t, P_]
+    L.fa_fp8_quantize.restype = ctypes.c_int
+    ws = P((1 << 20) * 256)
+    args = dict(B=2, H=4, Hkv=2, N=300, d=128, causal=0, scale=0.125)
+    def fwd(**kw):
+        a = dict(args, **kw)
+        return L.fa_fwd_fp8(kw.get("ws", ws), kw.get("nbytes", need), GOOD, GOOD, a["B"], a["H"], a["Hkv"], a["N"],
+                            a["d"], a["causal"], a["scale"], None)
+    assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(H=3) == fa.FA_ERR_INVALID_ARG
+    assert fwd(causal=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(nbytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert fwd(ws=P((1 << 20) * 256 + 16)) == fa.FA_ERR_MISALIGNED
+    assert fwd(B=0) == fa.FA_OK and fwd(N=0) == fa.FA_OK
+    assert L.fa_fp8_quantize(GOOD, GOOD, GOOD, None, 2, 4, 2, 300, 128, ws, need - 1, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_fp8_quantize(BAD, GOOD, GOOD, None, 2, 4, 2, 300, 128, ws, need, None) == fa.FA_ERR_MISALIGNED
+    assert L.fa_fp8_quantize(None, GOOD, GOOD, None, 2, 4, 2, 300, 128, ws, need, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fp8_quantize(GOOD, GOOD, GOOD, None, 2, 4, 2, 300, 64, ws, need, None) == fa.FA_ERR_UNSUPPORTED

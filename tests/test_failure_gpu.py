@@ -31,8 +31,11 @@ def _lib():
     fa.lib()
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
-    B, H, Hkv, N, d = 1, 1, 1, 512, 64
+@pytest.mark.parametrize("d,pair", [(64, 0), (128, 1)], ids=["1cta", "2cta"])
+def test_bounded_wait_reports_timeout_and_context_survives(d, pair):
+    B, H, Hkv, N = 1, 1, 1, 512
+    old_pair = fa.fa_get_option("fwd_2cta")
+    assert fa.fa_set_option("fwd_2cta", pair) == fa.FA_OK
     q, k, v, _ = make_inputs(B, H, Hkv, N, d, seed=5)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     assert fa.fa_last_device_status() == fa.FA_OK
@@ -48,6 +51,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     o, lse = fa.attention_forward(qd, kd, vd, causal=False)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
+    fa.fa_set_option("fwd_2cta", old_pair)
     o_ref, lse_ref = ref.attn_fwd(to64(q), to64(k), to64(v), False, d ** -0.5)
     assert o_error(to64(o), o_ref) <= O_TOL
     assert max_abs(to64(lse), lse_ref) <= LSE_TOL

@@ -27,6 +27,19 @@ def _lib():
     fa.lib()
 
 
+@pytest.fixture(autouse=True, params=[0, 1], ids=["1cta", "2cta"])
+def pair_mode(request):
+    """Every test runs on both forward kernels (one CTA per 256-row block, and CTA pairs over
+    512 rows with P in shared memory, used at head dimension 128) and both backward main-stage
+    kernels (one CTA per key tile, CTA pairs over 256 keys)."""
+    old = (fa.fa_get_option("fwd_2cta"), fa.fa_get_option("bwd_2cta"))
+    assert fa.fa_set_option("fwd_2cta", request.param) == fa.FA_OK
+    assert fa.fa_set_option("bwd_2cta", request.param) == fa.FA_OK
+    yield request.param
+    fa.fa_set_option("fwd_2cta", old[0])
+    fa.fa_set_option("bwd_2cta", old[1])
+
+
 def run_fwd(q, k, v, causal, scale):
     o, lse = fa.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
     torch.cuda.synchronize()
@@ -40,7 +53,8 @@ def check_full(B, H, Hkv, N, d, causal, seed, qk_mult=1.0):
     o, lse = run_fwd(q, k, v, causal, scale)
     o_ref, lse_ref = ref.attn_fwd(to64(q), to64(k), to64(v), causal, scale)
     eo, el = o_error(to64(o), o_ref), max_abs(to64(lse), lse_ref)
-    record("fwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=qk_mult, o_err=eo, lse_err=el,
+    record("fwd", shape=[B, H, Hkv, N, d], causal=bool(causal), qk_mult=qk_mult, pair=fa.fa_get_option("fwd_2cta"),
+           o_err=eo, lse_err=el,
            o_maxabs=max_abs(to64(o), o_ref), poly=fa.fa_get_option("poly_exp"),
            tau=fa.fa_get_option("rescale_threshold"))
     assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
@@ -112,7 +126,7 @@ def check_big_heads(w):
                                       to64(v[b:b + 1, g:g + 1]), w.causal, w.scale)
         eo = o_error(to64(o[b:b + 1, h:h + 1]), o_ref)
         el = max_abs(to64(lse[b:b + 1, h:h + 1]), lse_ref)
-        record("fwd_full_size", workload=w.name, head=[b, h], o_err=eo, lse_err=el,
+        record("fwd_full_size", workload=w.name, head=[b, h], pair=fa.fa_get_option("fwd_2cta"), o_err=eo, lse_err=el,
                o_maxabs=max_abs(to64(o[b:b + 1, h:h + 1]), o_ref))
         assert eo <= O_TOL and el <= LSE_TOL, ((b, h), eo, el)
 
@@ -135,7 +149,8 @@ def test_fwd_long_context_sampled_rows(N, d):
     o_ref, lse_ref = ref.attn_fwd(to64(qs), to64(k[:, heads]), to64(v[:, heads]), True, w.scale, qpos=rows)
     eo = o_error(to64(o[:, heads][:, :, rows]), o_ref)
     el = max_abs(to64(lse[:, heads][:, :, rows]), lse_ref)
-    record("fwd_long_context", workload=w.name, rows=int(len(rows)), heads=heads, o_err=eo, lse_err=el)
+    record("fwd_long_context", workload=w.name, rows=int(len(rows)), heads=heads, pair=fa.fa_get_option("fwd_2cta"),
+           o_err=eo, lse_err=el)
     assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
 
 

@@ -27,6 +27,19 @@ def _lib():
     fa.lib()
 
 
+@pytest.fixture(autouse=True, params=[0, 1], ids=["1cta", "2cta"])
+def pair_mode(request):
+    """Every test runs on both forward kernels (one CTA per 256-row block, and CTA pairs over
+    512 rows with P in shared memory, used at head dimension 128) and both backward main-stage
+    kernels (one CTA per key tile, CTA pairs over 256 keys)."""
+    old = (fa.fa_get_option("fwd_2cta"), fa.fa_get_option("bwd_2cta"))
+    assert fa.fa_set_option("fwd_2cta", request.param) == fa.FA_OK
+    assert fa.fa_set_option("bwd_2cta", request.param) == fa.FA_OK
+    yield request.param
+    fa.fa_set_option("fwd_2cta", old[0])
+    fa.fa_set_option("bwd_2cta", old[1])
+
+
 def _lse_err(lse, lse_ref):
     lse = to64(lse)
     masked = np.isneginf(lse_ref)
