@@ -467,10 +467,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 // Workspace layout, with the query rows of every head padded to Nqp = Nq rounded up to 128:
-// [dQ accumulator fp32 B*H*Nqp*d][lse2 fp32 B*H*Nqp][D fp32 B*H*Nqp][counters int32 B*H*Nqp/128]
+// [dQ accumulator fp32 B*H*Nqp*d][lse2 fp32 B*H*Nqp][D fp32 B*H*Nqp][counters int32]; the
+// deterministic mode's ordering counters: one per 128-row query tile (d = 64, 128), one per
+// 64-row query tile and head-dimension half (d = 256).
 struct BwdWorkspace {
   size_t off_lse2, off_d, off_cnt, total;
 };
+static size_t bwd_counter_count(size_t padded_rows, int d) {
+  return d == 256 ? padded_rows / 32 : padded_rows / 128;
+}
 static BwdWorkspace bwd_ws_layout(int B, int H, int Nq, int d, int deterministic) {
   const size_t Np = ((size_t)Nq + 127) / 128 * 128;
   const size_t rows = (size_t)B * H * Np;
@@ -479,12 +484,12 @@ static BwdWorkspace bwd_ws_layout(int B, int H, int Nq, int d, int deterministic
   w.off_lse2 = up(rows * d * 4);
   w.off_d = up(w.off_lse2 + rows * 4);
   w.off_cnt = up(w.off_d + rows * 4);
-  w.total = w.off_cnt + (deterministic ? up(rows / 128 * 4) : 0);
+  w.total = w.off_cnt + (deterministic ? up(bwd_counter_count(rows, d) * 4) : 0);
   return w;
 }
 
 size_t fa_bwd_qk_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int deterministic) {
-  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d) || d == 256) return 0;
+  if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d)) return 0;
   if (deterministic != 0 && deterministic != 1) return 0;
   return bwd_ws_layout(B, H, Nq, d, deterministic).total;
 }
@@ -499,7 +504,6 @@ static int check_bwd_common(int B, int H, int Hkv, int Nq, int d, int determinis
                             size_t ws_bytes) {
   int st = check_shape(B, H, Hkv, Nq, d);
   if (st) return st;
-  if (d == 256) return fail_detail(FA_ERR_UNSUPPORTED, "the backward supports d = 64 and 128");
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
   if (B == 0 || Nq == 0) return 1;
   if (!ws) return FA_ERR_WORKSPACE;
@@ -517,7 +521,8 @@ static int bwd_pre_impl(const void* o, const void* dout, const float* lse, int B
   cudaError_t e = launch_bwd_pre(d, o, dout, lse, reinterpret_cast<float*>(ws + w.off_lse2),
                                  reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws),
                                  deterministic ? reinterpret_cast<int*>(ws + w.off_cnt) : nullptr, heads, Nq,
-                                 heads * ((Nq + 127) / 128), static_cast<cudaStream_t>(stream));
+                                 (long long)bwd_counter_count((size_t)heads * ((Nq + 127) / 128 * 128), d),
+                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("fa_bwd_preprocess launch", e);
 }
 
@@ -554,7 +559,14 @@ static int bwd_main_impl(const void* q, const void* k, const void* v, const void
   if (!(p.kabort = abort_word_ptr())) return FA_ERR_CUDA;
   p.gen = next_generation();
   cudaError_t e;
-  if (d == 128 && options().bwd_2cta) {
+  if (d == 256) {
+    // 64-row query tiles (the four 64-column chunks of a row are loaded as separate boxes)
+    CUtensorMap tq64, tdo64;
+    if (make_tmap_bf16_rows(&tq64, q, d, Nq, (long long)B * H, 64) ||
+        make_tmap_bf16_rows(&tdo64, dout, d, Nq, (long long)B * H, 64))
+      return FA_ERR_CUDA;
+    e = launch_bwd256(tq64, tk, tv, tdo64, p, static_cast<cudaStream_t>(stream));
+  } else if (d == 128 && options().bwd_2cta) {
     CUtensorMap tq64, tdo64;
     if (make_tmap_bf16_rows(&tq64, q, d, Nq, (long long)B * H, 64) ||
         make_tmap_bf16_rows(&tdo64, dout, d, Nq, (long long)B * H, 64))

@@ -639,8 +639,12 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dout, const float* 
     bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
                                                  lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, heads,
                                                  N, Np, n_counters);
-  else
+  else if (d == 128)
     bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                                  lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, heads,
+                                                  N, Np, n_counters);
+  else
+    bwd_pre_kernel<256><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
                                                   lse, lse2, dvec, reinterpret_cast<float4*>(dq_acc), counters, heads,
                                                   N, Np, n_counters);
   return cudaGetLastError();

@@ -102,6 +102,9 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_bwd_main_pair(const CUtensorMap& tq, const CUtensorMap& tq64, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdo64,
                                  const BwdParams& p, cudaStream_t stream);
+// d = 256: two CTAs per key tile, one per head-dimension half (tq64, tdo64: 64-row boxes)
+cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo64, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
 // The forward on CTA pairs (d = 128, one split, MUFU exponentials): tq and tv with 128-row
 // boxes, tk64 with a 64-row box.

@@ -134,7 +134,10 @@ def test_workspace_size(L):
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, d, 1) > ws
     assert fa.fa_bwd_workspace_bytes(B, 3, 2, N, d, 0) == 0
     assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 96, 0) == 0
-    assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 256, 0) == 0
+    # d = 256: same accumulator layout; its counters are one per 64-row query tile and half
+    assert fa.fa_bwd_workspace_bytes(B, H, 2, N, 256, 0) >= B * H * N * 256 * 4 + B * H * N * 8
+    assert (fa.fa_bwd_workspace_bytes(B, H, 2, N, 256, 1) - fa.fa_bwd_workspace_bytes(B, H, 2, N, 256, 0)
+            >= B * H * N // 32 * 4)
     # rows are padded per head to a multiple of 128
     assert fa.fa_bwd_workspace_bytes(B, H, 2, 200, d, 0) == fa.fa_bwd_workspace_bytes(B, H, 2, 256, d, 0)
     assert fa.fa_bwd_workspace_bytes(B, H, 2, 1, d, 1) == fa.fa_bwd_workspace_bytes(B, H, 2, 128, d, 1)
@@ -148,7 +151,7 @@ def test_bwd_validation(L):
     assert bwd(q=None) == fa.FA_ERR_INVALID_ARG
     assert bwd(H=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
     assert bwd(d=80) == fa.FA_ERR_UNSUPPORTED
-    assert bwd(d=256) == fa.FA_ERR_UNSUPPORTED  # the backward supports d = 64 and 128
+    assert bwd(d=192) == fa.FA_ERR_UNSUPPORTED  # the backward supports d = 64, 128 and 256
     # any N is accepted; a ragged N needs the workspace of N rounded up to 128 rows per head
     assert bwd(N=200, wsb=fa.fa_bwd_workspace_bytes(1, 2, 1, 200, 64, 0) - 256) == fa.FA_ERR_WORKSPACE
     assert bwd(ws=None) == fa.FA_ERR_WORKSPACE
@@ -254,7 +257,7 @@ def test_noalloc_validates_like_fa_bwd(L):
     big_ws = 1 << 40  # any size: the checks below fail before the workspace size matters
     cases = [
         dict(d=96, N=0),                 # unsupported d even with no rows
-        dict(d=256, N=128),              # no backward at d = 256
+        dict(d=192, N=128),              # unsupported d with rows
         dict(H=3, Hkv=2),                # H % Hkv != 0
         dict(det=2),                     # bad deterministic flag
         dict(causal=2),                  # bad causal flag

@@ -9,8 +9,10 @@ The next call on the same context must work and be correct.
 
 The backward has two hooks ("debug_bwd_hook"): 1 makes the first CTA never
 release the deterministic mode's ordering counters, so the next key tile's
-bounded spin on the counter runs out; 2 makes the copy warp skip one Q/dO tile
-load, so the MMA warp's wait on that stage's mbarrier runs out.
+bounded spin on the counter runs out (at d = 256: the first pair of CTAs, both
+head-dimension halves of one key tile); 2 makes the copy warp skip one Q/dO tile
+load (at d = 256: stop loading after the first query tile), so the MMA warp's wait
+on that stage's mbarrier runs out.
 """
 import pytest
 import torch
@@ -57,10 +59,10 @@ def test_bounded_wait_reports_timeout_and_context_survives(d, pair):
     assert max_abs(to64(lse), lse_ref) <= LSE_TOL
 
 
-@pytest.mark.parametrize("pair", [0, 1], ids=["1cta", "2cta"])
+@pytest.mark.parametrize("d,pair", [(128, 0), (128, 1), (256, 0)], ids=["1cta", "2cta", "d256"])
 @pytest.mark.parametrize("hook,causal,det", [(1, True, True), (2, False, False)])
-def test_backward_bounded_waits_report_timeout(hook, causal, det, pair):
-    B, H, Hkv, N, d = 1, 1, 1, 512, 128
+def test_backward_bounded_waits_report_timeout(hook, causal, det, d, pair):
+    B, H, Hkv, N = 1, 1, 1, 512
     q, k, v, do = make_inputs(B, H, Hkv, N, d, seed=6)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal)

@@ -39,7 +39,8 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("d,causal,det", [(64, True, 0), (128, True, 0), (128, False, 1), (128, True, 1)])
+@pytest.mark.parametrize("d,causal,det", [(64, True, 0), (128, True, 0), (128, False, 1), (128, True, 1),
+                                           (256, True, 1)])
 def test_noalloc_matches_fa_bwd_twice(noalloc, d, causal, det):
     B, H, Hkv, N = 2, 4, 2, 512
     scale = d ** -0.5
