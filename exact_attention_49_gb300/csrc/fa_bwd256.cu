@@ -6,8 +6,9 @@
 // pair of CTAs per (b, K/V head, 128-key tile), CTA h owning head-dimension columns
 // [128 h, 128 h + 128).  Both recompute S^T = K Q^T and dP^T = V dO^T over all 256 columns
 // (that work is done twice); each accumulates its half of dV, dK and adds its half of dQ.
-// Query tiles are 64 rows so that K, V (64 KB each), one stage of Q and dO (32 KB each) and
-// dS^T fit in shared memory.  Per (query head of the group, 64-row query tile i):
+// Query tiles are 64 rows so that K, V (64 KB each), Q and dO (32 KB each, plus a second
+// buffer for the half of Q that dK reads) and dS^T fit in shared memory.  Per (query head of
+// the group, 64-row query tile i):
 //
 //   S^T  = K_j Q_i^T                (M = 128 keys, N = 64, K = 256)      TMEM
 //   dP^T = V_j dO_i^T               (M = 128, N = 64, K = 256)           TMEM
@@ -18,6 +19,14 @@
 //   dQ_i[:, h]^T = K_j[:, h]^T dS^T (M = 128, N = 64, K = 128 keys), its own TMEM columns,
 //                  read out and added with coalesced fp32 reductions (in a fixed order in
 //                  deterministic mode, one ordering counter per (head, query tile, half))
+//
+// Pipelining.  Each operand buffer is released by the last MMA that reads it, so the next
+// tile's copies overlap the current tile's work: the other half of Q (read by S^T only) after
+// S^T, the CTA's own half of Q (read by S^T and dK) into one of two buffers, the other half of
+// dO (read by dP^T only) after dP^T, the own half of dO (dP^T, dV) after dV, and the lse2/D
+// rows (two stages) after the compute warps' dS^T pass.  The MMA warp issues, per tile t:
+//   dV(t) | S^T(t+1) | dQ^T(t), dK(t) | dP^T(t+1)
+// so that the compute warps' P pass of tile t+1 overlaps the dQ and dK MMAs of tile t.
 //
 // Warp roles (512 threads): warps 0-7 compute (warpgroup w: queries 32 w .. 32 w + 31 of the
 // tile, thread = key row = TMEM lane), warps 8-11 dQ read-out then the dK/dV epilogue, warp 12
@@ -35,12 +44,15 @@ struct Bwd256Cfg {
   static constexpr int D = 256;
   static constexpr int OFF_K = 0;        // K_j [128 keys][256 d]: four chunks [128][64] of 16 KB
   static constexpr int OFF_V = 65536;
-  static constexpr int OFF_Q = 131072;   // Q_i [64 rows][256 d]: four chunks [64][64] of 8 KB
-  static constexpr int OFF_DO = 163840;
-  static constexpr int OFF_DS = 196608;  // dS^T [128 keys][64 queries]: one 16 KB chunk
-  static constexpr int OFF_LD = 212992;  // lse2[64] then D[64] (fp32)
-  static constexpr int OFF_BAR = 213504;
-  static constexpr int NBAR = 12;
+  // Q_i [64 rows][256 d] as four chunks [64][64] of 8 KB: the two chunks of the other half at
+  // OFF_QO, the CTA's own two chunks in one of two 16 KB buffers at OFF_QW
+  static constexpr int OFF_QO = 131072;
+  static constexpr int OFF_QW = 147456;
+  static constexpr int OFF_DO = 180224;  // dO_i: four chunks [64][64] in order
+  static constexpr int OFF_DS = 212992;  // dS^T [128 keys][64 queries]: one 16 KB chunk
+  static constexpr int OFF_LD = 229376;  // two stages of lse2[64] then D[64] (fp32)
+  static constexpr int OFF_BAR = 230400;
+  static constexpr int NBAR = 22;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384;
 };
@@ -77,9 +89,16 @@ __global__ void __launch_bounds__(512, 1)
     return;
   }
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = bar0 + 16;
-  const uint32_t s_full = bar0 + 24, dp_full = bar0 + 32, p_ready = bar0 + 40, ds_ready = bar0 + 48;
-  const uint32_t dq_full = bar0 + 56, dq_empty = bar0 + 64, mma_done = bar0 + 72;
+  const uint32_t kv_full = bar0;
+  const uint32_t qo_full = bar0 + 8, qo_empty = bar0 + 16;           // other half of Q
+  auto qw_full = [&](int s) { return bar0 + 24u + 8u * s; };       // own half of Q, two buffers
+  auto qw_empty = [&](int s) { return bar0 + 40u + 8u * s; };
+  auto ld_full = [&](int s) { return bar0 + 56u + 8u * s; };       // lse2/D rows, two stages
+  auto ld_empty = [&](int s) { return bar0 + 72u + 8u * s; };
+  const uint32_t doo_full = bar0 + 88, doo_empty = bar0 + 96;      // other half of dO
+  const uint32_t dow_full = bar0 + 104, dow_empty = bar0 + 112;    // own half of dO
+  const uint32_t s_full = bar0 + 120, dp_full = bar0 + 128, p_ready = bar0 + 136, ds_ready = bar0 + 144;
+  const uint32_t dq_full = bar0 + 152, dq_empty = bar0 + 160, mma_done = bar0 + 168;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const Abort ab{abort, p.status, p.kabort, p.gen};
@@ -112,8 +131,18 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 0 && lane == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(qo_full, 1);
+    mbar_init(qo_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qw_full(s), 1);
+      mbar_init(qw_empty(s), 1);
+      mbar_init(ld_full(s), 1);
+      mbar_init(ld_empty(s), 256);
+    }
+    mbar_init(doo_full, 1);
+    mbar_init(doo_empty, 1);
+    mbar_init(dow_full, 1);
+    mbar_init(dow_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
@@ -141,37 +170,62 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 13) {
     // ------------------------------------------------------------ TMA producer
+    // Copies of tile t, each after the buffer's previous reader is done, in the order those
+    // readers finish: other half of Q (S^T(t-1)), lse2/D (dS^T pass of t-2), own half of Q
+    // (dK(t-2)), other half of dO (dP^T(t-1)), own half of dO (dV(t-1)).
     if (lane == 0 && ntiles > 0) {
       mbar_arrive_expect_tx(kv_full, 2 * 65536);
       for (int ch = 0; ch < 4; ++ch) {
         tma_load_3d(sbase + C::OFF_K + ch * 16384, &tm_k, kv_full, ch * 64, j * 128, bg);
         tma_load_3d(sbase + C::OFF_V + ch * 16384, &tm_v, kv_full, ch * 64, j * 128, bg);
       }
+      const int oh = 1 - hh;  // the other half's chunks: 2 oh, 2 oh + 1
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
-        // single stage: the previous tile's MMAs have read Q, dO and the LSE/D rows
-        if (!mbar_wait(q_empty, (t & 1) ^ 1, ab)) break;
         if (p.debug_hook == 2 && t == 1) break;  // failure-injection test hook (never set in normal use)
-        const int bh = tile_head(t), i = tile_row(t);
-        mbar_arrive_expect_tx(q_full, 2 * 32768 + 512);
-        for (int ch = 0; ch < 4; ++ch) {
-          tma_load_3d(sbase + C::OFF_Q + ch * 8192, &tm_q, q_full, ch * 64, i * 64, bh);
-          tma_load_3d(sbase + C::OFF_DO + ch * 8192, &tm_do, q_full, ch * 64, i * 64, bh);
-        }
+        const int bh = tile_head(t), i = tile_row(t), s = t & 1;
+        const uint32_t pe = (t & 1) ^ 1, pe2 = ((t >> 1) & 1) ^ 1;
+        if (!mbar_wait(qo_empty, pe, ab)) break;
+        mbar_arrive_expect_tx(qo_full, 16384);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sbase + C::OFF_QO + c * 8192, &tm_q, qo_full, (2 * oh + c) * 64, i * 64, bh);
+        if (!mbar_wait(ld_empty(s), pe2, ab)) break;
         const size_t row0 = (size_t)bh * Np + (size_t)i * 64;
-        bulk_load256(sbase + C::OFF_LD, p.lse2 + row0, 256, q_full);
-        bulk_load256(sbase + C::OFF_LD + 256, p.dvec + row0, 256, q_full);
+        mbar_arrive_expect_tx(ld_full(s), 512);
+        bulk_load256(sbase + C::OFF_LD + s * 512, p.lse2 + row0, 256, ld_full(s));
+        bulk_load256(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row0, 256, ld_full(s));
+        if (!mbar_wait(qw_empty(s), pe2, ab)) break;
+        mbar_arrive_expect_tx(qw_full(s), 16384);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sbase + C::OFF_QW + s * 16384 + c * 8192, &tm_q, qw_full(s), (2 * hh + c) * 64, i * 64, bh);
+        if (!mbar_wait(doo_empty, pe, ab)) break;
+        mbar_arrive_expect_tx(doo_full, 16384);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sbase + C::OFF_DO + (2 * oh + c) * 8192, &tm_do, doo_full, (2 * oh + c) * 64, i * 64, bh);
+        if (!mbar_wait(dow_empty, pe, ab)) break;
+        mbar_arrive_expect_tx(dow_full, 16384);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sbase + C::OFF_DO + (2 * hh + c) * 8192, &tm_do, dow_full, (2 * hh + c) * 64, i * 64, bh);
         issued = t + 1;
       }
       if (*abort) {
-        if (issued > 0) {
+        // let copies in flight land before the CTA exits (bounded): the last tile's, and the
+        // tile before it in the two-buffer rings (a partly issued tile's copies are covered
+        // too: a barrier whose copies were not issued is not waited past its time limit)
+        auto drain = [&](uint32_t bar, uint32_t parity) {
           const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(q_full, (issued - 1) & 1) && globaltimer() - t0 < 1000000ull) {
+          while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < 1000000ull) {
           }
+        };
+        for (int t = max(0, issued - 2); t <= min(issued, ntiles - 1); ++t) {
+          const uint32_t pf = t & 1, pf2 = (t >> 1) & 1;
+          drain(qo_full, pf);
+          drain(ld_full(t & 1), pf2);
+          drain(qw_full(t & 1), pf2);
+          drain(doo_full, pf);
+          drain(dow_full, pf);
         }
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(kv_full, 0) && globaltimer() - t0 < 1000000ull) {
-        }
+        drain(kv_full, 0);
       }
     }
   } else if (warp == 12) {
@@ -180,33 +234,63 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16_f32(128, 128, false, true);  // dV, dK (B: MN-major)
       constexpr uint32_t idQ = idesc_bf16_f32(128, 64, true, true);     // dQ^T (A, B: MN-major)
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQ = sbase + C::OFF_Q;
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQO = sbase + C::OFF_QO;
       const uint32_t sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
-      // D[128 keys x 64 queries] = A[keys][256 d] . B[64 queries][256 d]^T, K-major
-      auto ss_full_d = [&](uint32_t dcol, uint32_t a, uint32_t bsm) {
+      auto sQW = [&](int t) { return sbase + C::OFF_QW + (t & 1) * 16384; };
+      // S^T(t) = K Q_t^T over the four head-dimension chunks (K-major A and B)
+      auto issue_s = [&](int t) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t qc = (c >> 1) == hh ? sQW(t) + (c & 1) * 8192 : sQO + (c & 1) * 8192;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            mma_ss(tmem + C::COL_S, sdesc_sw128(sK + c * 16384 + k4 * 32, 16, 1024),
+                   sdesc_sw128(qc + k4 * 32, 16, 1024), idS, (c | k4) != 0);
+        }
+      };
+      auto issue_dp = [&]() {  // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + dcol, sdesc_sw128(a + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(bsm + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
+          mma_ss(tmem + C::COL_DP, sdesc_sw128(sV + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(sDO + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
       };
-      bool ok = mbar_wait(kv_full, 0, ab);
+      auto wait_q = [&](int t) {
+        return mbar_wait(qo_full, t & 1, ab) && mbar_wait(qw_full(t & 1), (t >> 1) & 1, ab);
+      };
+      auto wait_do = [&](int t) { return mbar_wait(doo_full, t & 1, ab) && mbar_wait(dow_full, t & 1, ab); };
+      bool ok = mbar_wait(kv_full, 0, ab) && wait_q(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        mma_commit(s_full);
+        mma_commit(qo_empty);
+        ok = wait_do(0);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp();
+        mma_commit(dp_full);
+        mma_commit(doo_empty);
+      }
       for (int t = 0; ok && t < ntiles; ++t) {
         const uint32_t par = t & 1;
-        if (!(ok = mbar_wait(q_full, par, ab))) break;
-        tc_fence_after();
-        ss_full_d(C::COL_S, sK, sQ);
-        mma_commit(s_full);
-        ss_full_d(C::COL_DP, sV, sDO);
-        mma_commit(dp_full);
+        const bool more = t + 1 < ntiles;
         if (!(ok = mbar_wait(p_ready, par, ab))) break;
         tc_fence_after();
         // dV_h += P^T dO[:, h]: A = P^T from TMEM (16 queries = 8 columns per step; queries
-        // 32 w .. 32 w + 31 in columns 32 w .. 32 w + 15), B = dO's
-        // head-dimension chunks 2h, 2h+1 (MN-major, 8 KB apart)
+        // 32 w .. 32 w + 31 in columns 32 w .. 32 w + 15), B = dO's chunks 2h, 2h+1 (MN-major)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 32 * (kk >> 1) + (kk & 1) * 8,
                  sdesc_sw128(sDO + 2 * hh * 8192 + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(dow_empty);
+        if (more) {  // S^T of the next tile over the P^T columns (the dV MMAs above read them first)
+          if (!(ok = wait_q(t + 1))) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          mma_commit(s_full);
+          mma_commit(qo_empty);
+        }
         if (!(ok = mbar_wait(ds_ready, par, ab))) break;
         if (t > 0 && !(ok = mbar_wait(dq_empty, par ^ 1, ab))) break;
         tc_fence_after();
@@ -217,12 +301,19 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss(tmem + C::COL_DQ, sdesc_sw128(sK + 2 * hh * 16384 + kk * 2048, 16384, 1024),
                  sdesc_sw128(sDS + kk * 2048, 16384, 1024), idQ, kk > 0);
         mma_commit(dq_full);
-        // dK_h += dS^T Q[:, h]: A = dS^T (K-major over queries), B = Q's chunks 2h, 2h+1
+        // dK_h += dS^T Q[:, h]: A = dS^T (K-major over queries), B = this tile's own-half buffer
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + kk * 32, 16, 1024),
-                 sdesc_sw128(sQ + 2 * hh * 8192 + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(q_empty);  // Q, dO, dS^T and the LSE/D rows are free once these complete
+                 sdesc_sw128(sQW(t) + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(qw_empty(t & 1));
+        if (more) {  // dP^T of the next tile (the compute warps have read dP^T(t): ds_ready)
+          if (!(ok = wait_do(t + 1))) break;
+          tc_fence_after();
+          issue_dp();
+          mma_commit(dp_full);
+          mma_commit(doo_empty);
+        }
       }
       mma_commit(mma_done);
       const uint64_t t0 = globaltimer();
@@ -243,9 +334,10 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0; t < ntiles; ++t) {
       // causal: key 128 j + r is masked for query 64 i + 32 w + c when c < cut
       const int cut = p.causal ? r + 128 * j - 64 * tile_row(t) - 32 * w - p.qoff : 0;
-      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD) + 8 * w;
-      const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + 256) + 8 * w;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, ab))) break;
+      const int s = t & 1;
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512) + 8 * w;
+      const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512 + 256) + 8 * w;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, ab) && mbar_wait(ld_full(s), (t >> 1) & 1, ab))) break;
       tc_fence_after();
       float pv[32];
       {
@@ -315,6 +407,7 @@ __global__ void __launch_bounds__(512, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
+      mbar_arrive(ld_empty(s));  // this stage's lse2/D rows are no longer read
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ read-out, dK/dV epilogue
