@@ -45,10 +45,11 @@
  * that gives up (bounded at about 2 s) records FA_ERR_DEVICE_TIMEOUT in a
  * device status word, read and cleared by fa_last_device_status.
  *
- * Supported: d in {64, 128, 256} for the forward entry points and {64, 128}
- * for the backward (at d = 256 the backward's dK, dV accumulators alone would
- * fill tensor memory); H % Hkv == 0; 16-byte aligned bf16 pointers, 4-byte
- * aligned lse; any N >= 0; scale finite and > 0; an sm_103 device.
+ * Supported: d in {64, 128, 256} (the FP8 forward: d = 128); H % Hkv == 0;
+ * 16-byte aligned bf16 pointers, 4-byte aligned lse; any N >= 0; scale finite
+ * and > 0; an sm_103 device.  At d = 256 the backward's main stage runs two
+ * CTAs per 128-key tile, one per head-dimension half (a tile's dK and dV
+ * accumulators would otherwise fill tensor memory), on 64-row query tiles.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -107,7 +108,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * to Np = N rounded up to a multiple of 128: the fp32 dQ accumulator
  * [B,H,Np,d], one (LSE in log2 units, D) fp32 pair per padded query row, and
  * (deterministic mode) one int32 ordering counter per (b, h, 128-row query
- * block).  The workspace must be 256-byte aligned.  0 on bad sizes. */
+ * block), at d = 256 per (b, h, 64-row query block, head-dimension half).
+ * The workspace must be 256-byte aligned.  0 on bad sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int deterministic);
 
 /* Backward: dq, dk, dv (bf16) from q, k, v, o, dout (bf16) and lse (fp32, as
@@ -246,11 +248,13 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *                        returns FA_ERR_DEVICE_TIMEOUT.  Output is undefined
  *                        while it is set.
  *   "debug_bwd_hook"     failure-injection test hook of the backward, 0
- *                        (default), 1 (the first CTA never releases the
- *                        deterministic mode's ordering counters, so the next
- *                        key tile's bounded spin gives up) or 2 (the copy warp
- *                        skips the second query tile's Q/dO load, so the MMA
- *                        warp's bounded wait gives up); then as above.
+ *                        (default), 1 (the first CTA, at d = 256 the first
+ *                        two, never releases the deterministic mode's ordering
+ *                        counters, so the next key tile's bounded spin gives
+ *                        up) or 2 (the copy warp skips the second query tile's
+ *                        Q/dO load, at d = 256 every load from the second
+ *                        tile on, so the MMA warp's bounded wait gives up);
+ *                        then as above.
  * Returns FA_OK, FA_ERR_INVALID_ARG (unknown key or value out of range) or,
  * for "rescale_events", FA_ERR_CUDA. */
 int fa_set_option(const char* key, double value);
