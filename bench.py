@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -68,9 +69,9 @@ KERNEL_SOURCES = {
 }
 
 
-def dram_traffic(kernel):
+def dram_traffic(kernel, workload_name):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current source of that kernel (else None)."""
+    the current source of that kernel and scaled to this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -78,6 +79,8 @@ def dram_traffic(kernel):
     except (OSError, ValueError):
         return None
     if not rec or rec.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    if rec.get("full_workload") != workload_name:
         return None
     return rec.get("bytes_per_launch_full_workload")
 
@@ -237,8 +240,8 @@ def config_of(w, fwd_only=False):
     return {"workload": w.name + (", forward only" if fwd_only else ", forward + backward"), "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
             "d": w.d, "causal": w.causal, "softmax_scale": "1/sqrt(d)", "seed": w.seed,
             "inputs": "Q,K,V,dO i.i.d. N(0,1) rounded to bf16",
-            "l2": "inputs larger than L2: each of Q,K,V,O,dO,dQ,dK,dV is %d MiB (L2 is 129 MB)"
-                  % (w.B * w.H * w.N * w.d * 2 >> 20),
+            "l2": "inputs larger than L2: Q,K,V,dO together %d MiB, each of Q,K,V,O,dO,dQ,dK,dV %d MiB "
+                  "(L2 is 129 MB)" % (4 * w.B * w.H * w.N * w.d * 2 >> 20, w.B * w.H * w.N * w.d * 2 >> 20),
             "parallelism": "replicas"}
 
 
@@ -335,38 +338,92 @@ def run_ours(args, w):
     f_bwd = 0.0 if fwd_only else 2.5 * f_fwd
     value = throughput_tflops(f_fwd + f_bwd, ws, args.steps, total_ms)
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region.
+    # Every step copies its four inputs from pinned host memory and reads its five results back
+    # into pinned host memory.  The copies run on their own streams, on two sets of device and
+    # host buffers, so step i's host-to-device copies overlap step i-1's kernels and step i-1's
+    # read-back overlaps step i's kernels (the usual copy/compute pipeline of a training or
+    # serving loop); the timed region runs from before the first copy to the end of the last
+    # read-back.
     ins = (q_h, k_h, v_h) if fwd_only else (q_h, k_h, v_h, do_h)
-    hq, hk, hv = (x.pin_memory() for x in (q_h, k_h, v_h))
-    hdo = do_h.pin_memory() if not fwd_only else None
-    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q_h, q_h, k_h, v_h))
-    hlse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
-    outs = (ho, hlse) if fwd_only else (ho, hlse, hdq, hdk, hdv)
     h2d = sum(x.numel() * x.element_size() for x in ins)
-    d2h = sum(x.numel() * x.element_size() for x in outs)
-    e2e_steps = max(3, min(args.steps, 20))
-
-    def e2e_step():
-        for dst, src in zip((q, k, v, do), (hq, hk, hv, hdo)):
-            if src is not None:
-                dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in zip(outs, (o, lse, dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
-
+    out_shapes = [(q_h.shape, q_h.dtype), ((B, H, N), torch.float32)]
+    if not fwd_only:
+        out_shapes += [(q_h.shape, q_h.dtype), (k_h.shape, k_h.dtype), (v_h.shape, v_h.dtype)]
+    d2h = sum(math.prod(sh) * torch.empty((), dtype=dt).element_size() for sh, dt in out_shapes)
+    e2e_steps = max(4, min(args.steps, 40))
     e2e_value = None
     if not args.no_e2e:
-        e2e_step()
+        h_in = [x.pin_memory() for x in ins]
+        sets = []
+        for _ in range(2):
+            d_in = [torch.empty_like(x, device=dev) for x in ins]
+            d_out = [torch.empty(sh, dtype=dt, device=dev) for sh, dt in out_shapes]
+            h_out = [torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in out_shapes]
+            sets.append((d_in, d_out, h_out))
+        s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+        def e2e_compute(d_in, d_out):
+            qq, kk, vv = d_in[:3]
+            oo, ll = d_out[:2]
+            check("fa_fwd", fa.fa_fwd(qq, kk, vv, oo, ll, B, H, Hkv, N, d, causal, scale, stream))
+            if fwd_only:
+                return
+            dd = d_in[3]
+            gq, gk, gv = d_out[2:]
+            check("fa_bwd_preprocess", fa.fa_bwd_preprocess(oo, dd, ll, B, H, Hkv, N, d, det, wsp, ws_bytes, stream))
+            check("fa_bwd_main", fa.fa_bwd_main(qq, kk, vv, dd, ll, gk, gv, B, H, Hkv, N, d, causal, scale, det, wsp,
+                                                ws_bytes, stream))
+            check("fa_bwd_postprocess", fa.fa_bwd_postprocess(gq, B, H, Hkv, N, d, det, wsp, ws_bytes, stream))
+
+        def e2e_run(n):
+            in_free = [None, None]   # compute of the step that last used the set's inputs is done
+            out_free = [None, None]  # read-back of the step that last used the set's outputs is done
+            begin = torch.cuda.Event()
+            begin.record(stream)
+            s_h2d.wait_event(begin)
+            last = None
+            for i in range(n):
+                d_in, d_out, h_out = sets[i & 1]
+                with torch.cuda.stream(s_h2d):
+                    if in_free[i & 1] is not None:
+                        s_h2d.wait_event(in_free[i & 1])
+                    for dst, src in zip(d_in, h_in):
+                        dst.copy_(src, non_blocking=True)
+                    ready = torch.cuda.Event()
+                    ready.record(s_h2d)
+                stream.wait_event(ready)
+                if out_free[i & 1] is not None:
+                    stream.wait_event(out_free[i & 1])
+                e2e_compute(d_in, d_out)
+                done = torch.cuda.Event()
+                done.record(stream)
+                in_free[i & 1] = done
+                with torch.cuda.stream(s_d2h):
+                    s_d2h.wait_event(done)
+                    for dst, src in zip(h_out, d_out):
+                        dst.copy_(src, non_blocking=True)
+                    last = torch.cuda.Event()
+                    last.record(s_d2h)
+                out_free[i & 1] = last
+            stream.wait_event(last)
+
+        e2e_run(2)
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        e2e_run(e2e_steps)
         e1.record(stream)
         torch.cuda.synchronize()
+        st = fa.fa_last_device_status(stream)
+        if st != fa.FA_OK:
+            raise fa.FAError("device status after the end-to-end steps", st)
         e2e_value = throughput_tflops(f_fwd + f_bwd, ws, e2e_steps, max_over_ranks(e0.elapsed_time(e1), dev))
+        # the pipelined results are the step's results: the last read-back equals the device-resident run
+        if not torch.equal(sets[(e2e_steps - 1) & 1][2][0], o.cpu()):
+            raise SystemExit("end-to-end output differs from the device-resident step")
 
     if rank != 0:
         if ws > 1:
@@ -381,8 +438,11 @@ def run_ours(args, w):
     dom_ms = main_ms if dominant == "bwd_main" else fwd_ms
     dom_flops = f_bwd if dominant == "bwd_main" else f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": dram_traffic(dominant),
+    dom_kernel = {"fwd": "fwd_kernel<%d, 0>" % d,
+                  "bwd_main": "bwd256_kernel" if d == 256 else "bwd_main_kernel<%d>" % d}[dominant]
+    roofline = {"bound": "tensor", "kernel": dom_kernel, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": dram_traffic(dominant, w.name) if d == 128 and not det else None,
                 "peak_source": "%s %s (%s)" % (peak_src, peak_key, "MEASURED_PEAKS.json" if peak_src == "measured"
                                                else "profiling recipe fallback")}
 
@@ -406,7 +466,9 @@ def run_ours(args, w):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                                               "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                                               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                                               "copies": "pinned host buffers, own streams, overlapped with the "
+                                                         "neighbouring steps' kernels"},
         "gpu_launches": (1 if fwd_only else 4) * args.steps,
         "poly_exp": fa.fa_get_option("poly_exp"),
         "bwd_2cta": fa.fa_get_option("bwd_2cta"),

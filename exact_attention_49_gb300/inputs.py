@@ -43,6 +43,8 @@ WORKLOADS = {
     "C3b": Workload("C3b B4 H16 N8192 d128 causal, Q and K x4", 4, 16, 16, 8192, 128, True,
                     qk_mult=4.0, seed=3),
     "C4": Workload("C4 GQA B2 Hq32 Hkv8 N16384 d128 causal", 2, 32, 8, 16384, 128, True, seed=4),
+    # head dimension 256, forward and backward (the wider-head shape of the general-shape row)
+    "HD256": Workload("HD256 B1 H16 N8192 d256 causal", 1, 16, 16, 8192, 256, True, seed=6),
 }
 
 
