@@ -113,19 +113,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
   const int gi = cl / (kHeadGroup * npair);
   const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
   const int rem = cl - gi * kHeadGroup * npair;
-  const bool desc = p.deterministic && p.causal;
+  const int grp = p.H / p.Hkv;
+  // deterministic causal schedules as in fa_bwd.cu, by key pairs
+  const bool det_causal = p.deterministic && p.causal;
+  const bool desc = det_causal && grp == 1;
+  const bool interleave = det_causal && grp > 1;
   const int jp = desc ? npair - 1 - rem / gsz : rem / gsz;
   const int bg = gi * kHeadGroup + rem % gsz;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int grp = p.H / p.Hkv;
   const int j = 2 * jp + (int)rank;
   // causal: the first query tile with a row at or after the pair's first key 256 jp
   const int first = 256 * jp - 127 - p.qoff;
   const int i0 = (p.causal && first > 0) ? (first + 127) / 128 : 0;
   const int ni = max(nq - i0, 0);
   const int ntiles = aligned_ok ? grp * ni : 0;
-  auto tile_head = [&](int t) { return b * p.H + g * grp + t / ni; };
-  auto tile_row = [&](int t) { return i0 + t % ni; };
+  auto tile_head = [&](int t) { return b * p.H + g * grp + (interleave ? t % grp : t / ni); };
+  auto tile_row = [&](int t) { return interleave ? nq - 1 - t / grp : i0 + t % ni; };
 
   if (warp == 0 && lane == 0) {
     mbar_init(kv_full, 1);

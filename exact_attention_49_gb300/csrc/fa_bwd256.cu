@@ -116,18 +116,21 @@ __global__ void __launch_bounds__(512, 1)
   const int gi = cta / (kHeadGroup * nkv);
   const int gsz = min(kHeadGroup, BG - gi * kHeadGroup);
   const int rem = cta - gi * kHeadGroup * nkv;
-  const bool desc = p.deterministic && p.causal;
+  const int grp = p.H / p.Hkv;
+  // deterministic causal schedules as in fa_bwd.cu
+  const bool det_causal = p.deterministic && p.causal;
+  const bool desc = det_causal && grp == 1;
+  const bool interleave = det_causal && grp > 1;
   const int j = desc ? nkv - 1 - rem / gsz : rem / gsz;
   const int bg = gi * kHeadGroup + rem % gsz;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int grp = p.H / p.Hkv;
   // causal: the first 64-row query tile with a row at or after key 128 j
   const int first = 128 * j - 63 - p.qoff;
   const int i0 = (p.causal && first > 0) ? (first + 63) / 64 : 0;
   const int ni = max(nq - i0, 0);
   const int ntiles = grp * ni;
-  auto tile_head = [&](int t) { return b * p.H + g * grp + t / ni; };
-  auto tile_row = [&](int t) { return i0 + t % ni; };
+  auto tile_head = [&](int t) { return b * p.H + g * grp + (interleave ? t % grp : t / ni); };
+  auto tile_row = [&](int t) { return interleave ? nq - 1 - t / grp : i0 + t % ni; };
 
   if (warp == 0 && lane == 0) {
     mbar_init(kv_full, 1);
@@ -421,8 +424,9 @@ __global__ void __launch_bounds__(512, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, ab));
       if (!ok) break;
       tc_fence_after();
-      // deterministic: one counter per (head, 64-row query tile, half); contributions in key
-      // tile order (descending from the last key tile the query tile sees under a causal mask)
+      // deterministic: one counter per (head, 64-row query tile, half); contributions in the
+      // order of the schedule (ascending key tiles, or descending from the last one the query
+      // tile sees)
       int* counter = p.deterministic ? p.counters + (((size_t)bh * nq + i) * 2 + hh) : nullptr;
       const int rank = desc ? min(nkv - 1, (64 * i + 63 + p.qoff) / 128) - j : j;
       if (p.deterministic) {

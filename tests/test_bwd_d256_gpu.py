@@ -90,10 +90,11 @@ def test_bwd_d256_nq_ne_nk(Nq, Nk):
         assert torch.all(dq[:, :, :Nq - Nk] == 0)
 
 
+@pytest.mark.parametrize("Hkv", [2, 8], ids=["grouped", "one_head_per_group"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_d256_deterministic_bit_identical(causal):
-    outs, refs = _run(2, 8, 2, 1024, 1024, causal, seed=740, det=True, repeats=3)
-    _check(outs, refs, [2, 8, 2, 1024, D], causal, True)
+def test_bwd_d256_deterministic_bit_identical(causal, Hkv):
+    outs, refs = _run(2, 8, Hkv, 1024, 1024, causal, seed=740, det=True, repeats=3)
+    _check(outs, refs, [2, 8, Hkv, 1024, D], causal, True)
     for again in outs[1:]:
         for a, b in zip(outs[0], again):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -112,6 +112,20 @@ def test_bwd_ragged(N, causal, d):
     assert max(rows) <= ROW_TOL, rows
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_deterministic_one_head_per_group(causal, d):
+    """Deterministic mode without grouped heads: under a causal mask the contributions run in
+    descending key-tile order (the schedule for H == Hkv); ragged N, bit-identical reruns."""
+    B, H, Hkv, N = 2, 4, 4, 700
+    check_full(B, H, Hkv, N, d, causal, seed=29 + d, deterministic=True)
+    q, k, v, do = make_inputs(B, H, Hkv, N, d, seed=29 + d)
+    first = gpu_fwd_bwd(q, k, v, do, causal, d ** -0.5, deterministic=True)
+    again = gpu_fwd_bwd(q, k, v, do, causal, d ** -0.5, deterministic=True)
+    for a, b in zip(first, again):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 @pytest.mark.parametrize("det", [False, True])
 def test_bwd_ragged_gqa(det):
     check_full(2, 8, 2, 700, 128, True, seed=23, deterministic=det)
