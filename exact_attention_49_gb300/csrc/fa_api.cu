@@ -537,6 +537,7 @@ static int bwd_main_impl(const void* q, const void* k, const void* v, const void
   const BwdWorkspace w = bwd_ws_layout(B, H, Nq, d, deterministic);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdParams p{};
+  p.v = v;
   p.dk = dk;
   p.dv = dv;
   p.dq_acc = reinterpret_cast<float*>(ws);
@@ -565,7 +566,7 @@ static int bwd_main_impl(const void* q, const void* k, const void* v, const void
     if (make_tmap_bf16_rows(&tq64, q, d, Nq, (long long)B * H, 64) ||
         make_tmap_bf16_rows(&tdo64, dout, d, Nq, (long long)B * H, 64))
       return FA_ERR_CUDA;
-    e = launch_bwd256(tq64, tk, tv, tdo64, p, static_cast<cudaStream_t>(stream));
+    e = launch_bwd256(tq64, tk, tdo64, p, static_cast<cudaStream_t>(stream));
   } else if (d == 128 && options().bwd_2cta) {
     CUtensorMap tq64, tdo64;
     if (make_tmap_bf16_rows(&tq64, q, d, Nq, (long long)B * H, 64) ||

@@ -6,32 +6,29 @@
 // pair of CTAs per (b, K/V head, 128-key tile), CTA h owning head-dimension columns
 // [128 h, 128 h + 128).  Both recompute S^T = K Q^T and dP^T = V dO^T over all 256 columns
 // (that work is done twice); each accumulates its half of dV, dK and adds its half of dQ.
-// Query tiles are 64 rows so that K, V (64 KB each), Q and dO (32 KB each, plus a second
-// buffer for the half of Q that dK reads) and dS^T fit in shared memory.  Per (query head of
-// the group, 64-row query tile i):
+// Per (query head of the group, 64-row query tile i):
 //
 //   S^T  = K_j Q_i^T                (M = 128 keys, N = 64, K = 256)      TMEM
-//   dP^T = V_j dO_i^T               (M = 128, N = 64, K = 256)           TMEM
+//   dP^T = V_j dO_i^T               (M = 128, N = 64, K = 256; A = V_j from TMEM)
 //   P^T  = exp2(S^T scale log2e - lse2_i)  (bf16, over S^T)
 //   dS^T = P^T (dP^T - D_i) scale          (bf16, shared memory)
 //   dV_h += P^T dO_i[:, h]          (M = 128, N = 128, K = 64; A from TMEM)
 //   dK_h += dS^T Q_i[:, h]          (M = 128, N = 128, K = 64)
-//   dQ_i[:, h]^T = K_j[:, h]^T dS^T (M = 128, N = 64, K = 128 keys), its own TMEM columns,
+//   dQ_i[:, h]^T = K_j[:, h]^T dS^T (M = 128, N = 64, K = 128 keys), into the dP^T columns,
 //                  read out and added with coalesced fp32 reductions (in a fixed order in
 //                  deterministic mode, one ordering counter per (head, query tile, half))
 //
-// Pipelining.  Each operand buffer is released by the last MMA that reads it, so the next
-// tile's copies overlap the current tile's work: the other half of Q (read by S^T only) after
-// S^T, the CTA's own half of Q (read by S^T and dK) into one of two buffers, the other half of
-// dO (read by dP^T only) after dP^T, the own half of dO (dP^T, dV) after dV, and the lse2/D
-// rows (two stages) after the compute warps' dS^T pass.  The MMA warp issues, per tile t:
-//   dV(t) | S^T(t+1) | dQ^T(t), dK(t) | dP^T(t+1)
-// so that the compute warps' P pass of tile t+1 overlaps the dQ and dK MMAs of tile t.
+// V_j is read by one GEMM only, so it lives in tensor memory (written once per CTA by the
+// compute warps from plain loads) as dP^T's A operand.  That leaves K_j and two stages of
+// Q_i and dO_i (32 KB each per stage) in shared memory, so the next tile's copies overlap the
+// current tile.  The MMA warp issues, per tile t:
+//   dV(t) | S^T(t+1) | dQ^T(t), dK(t) | dP^T(t+1) once dQ^T(t) has been read out
+// so the compute warps' P pass of tile t+1 overlaps the dQ and dK MMAs of tile t.
 //
 // Warp roles (512 threads): warps 0-7 compute (warpgroup w: queries 32 w .. 32 w + 31 of the
 // tile, thread = key row = TMEM lane), warps 8-11 dQ read-out then the dK/dV epilogue, warp 12
 // MMA issue and TMEM allocation, warp 13 TMA producer, warps 14-15 idle.
-// Tensor memory: dV_h | dK_h | S^T (then P^T) | dP^T | dQ^T (448 of 512 columns).
+// Tensor memory: dV_h | dK_h | S^T (then P^T) | dP^T (then dQ^T_h) | V_j (512 columns).
 #include <algorithm>
 #include <type_traits>
 
@@ -43,18 +40,15 @@ namespace fa {
 struct Bwd256Cfg {
   static constexpr int D = 256;
   static constexpr int OFF_K = 0;        // K_j [128 keys][256 d]: four chunks [128][64] of 16 KB
-  static constexpr int OFF_V = 65536;
-  // Q_i [64 rows][256 d] as four chunks [64][64] of 8 KB: the two chunks of the other half at
-  // OFF_QO, the CTA's own two chunks in one of two 16 KB buffers at OFF_QW
-  static constexpr int OFF_QO = 131072;
-  static constexpr int OFF_QW = 147456;
-  static constexpr int OFF_DO = 180224;  // dO_i: four chunks [64][64] in order
-  static constexpr int OFF_DS = 212992;  // dS^T [128 keys][64 queries]: one 16 KB chunk
-  static constexpr int OFF_LD = 229376;  // two stages of lse2[64] then D[64] (fp32)
-  static constexpr int OFF_BAR = 230400;
-  static constexpr int NBAR = 22;
+  static constexpr int OFF_Q = 65536;    // two stages of Q_i [64 rows][256 d]: four chunks [64][64] of 8 KB
+  static constexpr int OFF_DO = 131072;  // two stages of dO_i, same layout
+  static constexpr int STAGE = 32768;
+  static constexpr int OFF_DS = 196608;  // dS^T [128 keys][64 queries]: one 16 KB chunk
+  static constexpr int OFF_LD = 212992;  // two stages of lse2[64] then D[64] (fp32)
+  static constexpr int OFF_BAR = 214016;
+  static constexpr int NBAR = 14;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384;
+  static constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_V = 384;
 };
 
 FA_DEV void bulk_load256(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -73,11 +67,17 @@ FA_DEV int ld_acquire256(const int* p) {
 FA_DEV void st_release256(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+FA_DEV uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __global__ void __launch_bounds__(512, 1)
     bwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using C = Bwd256Cfg;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -89,16 +89,11 @@ __global__ void __launch_bounds__(512, 1)
     return;
   }
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t kv_full = bar0;
-  const uint32_t qo_full = bar0 + 8, qo_empty = bar0 + 16;           // other half of Q
-  auto qw_full = [&](int s) { return bar0 + 24u + 8u * s; };       // own half of Q, two buffers
-  auto qw_empty = [&](int s) { return bar0 + 40u + 8u * s; };
-  auto ld_full = [&](int s) { return bar0 + 56u + 8u * s; };       // lse2/D rows, two stages
-  auto ld_empty = [&](int s) { return bar0 + 72u + 8u * s; };
-  const uint32_t doo_full = bar0 + 88, doo_empty = bar0 + 96;      // other half of dO
-  const uint32_t dow_full = bar0 + 104, dow_empty = bar0 + 112;    // own half of dO
-  const uint32_t s_full = bar0 + 120, dp_full = bar0 + 128, p_ready = bar0 + 136, ds_ready = bar0 + 144;
-  const uint32_t dq_full = bar0 + 152, dq_empty = bar0 + 160, mma_done = bar0 + 168;
+  const uint32_t k_full = bar0;
+  auto st_full = [&](int s) { return bar0 + 8u + 8u * s; };    // Q, dO, lse2/D of one stage
+  auto st_empty = [&](int s) { return bar0 + 24u + 8u * s; };
+  const uint32_t s_full = bar0 + 40, dp_full = bar0 + 48, p_ready = bar0 + 56, ds_ready = bar0 + 64;
+  const uint32_t dq_full = bar0 + 72, dq_empty = bar0 + 80, v_ready = bar0 + 88, mma_done = bar0 + 96;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const Abort ab{abort, p.status, p.kabort, p.gen};
@@ -133,25 +128,18 @@ __global__ void __launch_bounds__(512, 1)
   auto tile_row = [&](int t) { return interleave ? nq - 1 - t / grp : i0 + t % ni; };
 
   if (warp == 0 && lane == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(qo_full, 1);
-    mbar_init(qo_empty, 1);
+    mbar_init(k_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(qw_full(s), 1);
-      mbar_init(qw_empty(s), 1);
-      mbar_init(ld_full(s), 1);
-      mbar_init(ld_empty(s), 256);
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
     }
-    mbar_init(doo_full, 1);
-    mbar_init(doo_empty, 1);
-    mbar_init(dow_full, 1);
-    mbar_init(dow_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
+    mbar_init(v_ready, 256);
     mbar_init(mma_done, 1);
     *abort = 0;
     fence_mbar_init();
@@ -163,7 +151,6 @@ __global__ void __launch_bounds__(512, 1)
   if (warp == 13 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
   }
   tc_fence_before();
@@ -173,107 +160,70 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 13) {
     // ------------------------------------------------------------ TMA producer
-    // Copies of tile t, each after the buffer's previous reader is done, in the order those
-    // readers finish: other half of Q (S^T(t-1)), lse2/D (dS^T pass of t-2), own half of Q
-    // (dK(t-2)), other half of dO (dP^T(t-1)), own half of dO (dV(t-1)).
     if (lane == 0 && ntiles > 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * 65536);
-      for (int ch = 0; ch < 4; ++ch) {
-        tma_load_3d(sbase + C::OFF_K + ch * 16384, &tm_k, kv_full, ch * 64, j * 128, bg);
-        tma_load_3d(sbase + C::OFF_V + ch * 16384, &tm_v, kv_full, ch * 64, j * 128, bg);
-      }
-      const int oh = 1 - hh;  // the other half's chunks: 2 oh, 2 oh + 1
+      mbar_arrive_expect_tx(k_full, 65536);
+      for (int ch = 0; ch < 4; ++ch)
+        tma_load_3d(sbase + C::OFF_K + ch * 16384, &tm_k, k_full, ch * 64, j * 128, bg);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
+        const int s = t & 1;
         if (p.debug_hook == 2 && t == 1) break;  // failure-injection test hook (never set in normal use)
-        const int bh = tile_head(t), i = tile_row(t), s = t & 1;
-        const uint32_t pe = (t & 1) ^ 1, pe2 = ((t >> 1) & 1) ^ 1;
-        if (!mbar_wait(qo_empty, pe, ab)) break;
-        mbar_arrive_expect_tx(qo_full, 16384);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sbase + C::OFF_QO + c * 8192, &tm_q, qo_full, (2 * oh + c) * 64, i * 64, bh);
-        if (!mbar_wait(ld_empty(s), pe2, ab)) break;
+        // the stage's previous tile (t - 2) is done: its dK MMA, the last reader, completed
+        if (!mbar_wait(st_empty(s), ((t >> 1) & 1) ^ 1, ab)) break;
+        const int bh = tile_head(t), i = tile_row(t);
+        mbar_arrive_expect_tx(st_full(s), 2 * C::STAGE + 512);
+        for (int ch = 0; ch < 4; ++ch) {
+          tma_load_3d(sbase + C::OFF_Q + s * C::STAGE + ch * 8192, &tm_q, st_full(s), ch * 64, i * 64, bh);
+          tma_load_3d(sbase + C::OFF_DO + s * C::STAGE + ch * 8192, &tm_do, st_full(s), ch * 64, i * 64, bh);
+        }
         const size_t row0 = (size_t)bh * Np + (size_t)i * 64;
-        mbar_arrive_expect_tx(ld_full(s), 512);
-        bulk_load256(sbase + C::OFF_LD + s * 512, p.lse2 + row0, 256, ld_full(s));
-        bulk_load256(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row0, 256, ld_full(s));
-        if (!mbar_wait(qw_empty(s), pe2, ab)) break;
-        mbar_arrive_expect_tx(qw_full(s), 16384);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sbase + C::OFF_QW + s * 16384 + c * 8192, &tm_q, qw_full(s), (2 * hh + c) * 64, i * 64, bh);
-        if (!mbar_wait(doo_empty, pe, ab)) break;
-        mbar_arrive_expect_tx(doo_full, 16384);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sbase + C::OFF_DO + (2 * oh + c) * 8192, &tm_do, doo_full, (2 * oh + c) * 64, i * 64, bh);
-        if (!mbar_wait(dow_empty, pe, ab)) break;
-        mbar_arrive_expect_tx(dow_full, 16384);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sbase + C::OFF_DO + (2 * hh + c) * 8192, &tm_do, dow_full, (2 * hh + c) * 64, i * 64, bh);
+        bulk_load256(sbase + C::OFF_LD + s * 512, p.lse2 + row0, 256, st_full(s));
+        bulk_load256(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row0, 256, st_full(s));
         issued = t + 1;
       }
-      if (*abort) {
-        // let copies in flight land before the CTA exits (bounded): the last tile's, and the
-        // tile before it in the two-buffer rings (a partly issued tile's copies are covered
-        // too: a barrier whose copies were not issued is not waited past its time limit)
-        auto drain = [&](uint32_t bar, uint32_t parity) {
+      if (*abort) {  // let copies in flight land before the CTA exits (bounded)
+        for (int t = max(0, issued - 2); t < issued; ++t) {
           const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < 1000000ull) {
+          while (!mbar_try_wait(st_full(t & 1), (t >> 1) & 1) && globaltimer() - t0 < 1000000ull) {
           }
-        };
-        for (int t = max(0, issued - 2); t <= min(issued, ntiles - 1); ++t) {
-          const uint32_t pf = t & 1, pf2 = (t >> 1) & 1;
-          drain(qo_full, pf);
-          drain(ld_full(t & 1), pf2);
-          drain(qw_full(t & 1), pf2);
-          drain(doo_full, pf);
-          drain(dow_full, pf);
         }
-        drain(kv_full, 0);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(k_full, 0) && globaltimer() - t0 < 1000000ull) {
+        }
       }
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------ MMA issuer (one lane)
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T (K-major)
       constexpr uint32_t idKV = idesc_bf16_f32(128, 128, false, true);  // dV, dK (B: MN-major)
       constexpr uint32_t idQ = idesc_bf16_f32(128, 64, true, true);     // dQ^T (A, B: MN-major)
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQO = sbase + C::OFF_QO;
-      const uint32_t sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
-      auto sQW = [&](int t) { return sbase + C::OFF_QW + (t & 1) * 16384; };
-      // S^T(t) = K Q_t^T over the four head-dimension chunks (K-major A and B)
-      auto issue_s = [&](int t) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t qc = (c >> 1) == hh ? sQW(t) + (c & 1) * 8192 : sQO + (c & 1) * 8192;
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            mma_ss(tmem + C::COL_S, sdesc_sw128(sK + c * 16384 + k4 * 32, 16, 1024),
-                   sdesc_sw128(qc + k4 * 32, 16, 1024), idS, (c | k4) != 0);
-        }
-      };
-      auto issue_dp = [&]() {  // dP^T = V dO^T
+      const uint32_t sK = sbase + C::OFF_K, sDS = sbase + C::OFF_DS;
+      auto sQ = [&](int t) { return sbase + C::OFF_Q + (t & 1) * C::STAGE; };
+      auto sDO = [&](int t) { return sbase + C::OFF_DO + (t & 1) * C::STAGE; };
+      auto issue_s = [&](int t) {  // S^T = K Q_t^T over the four head-dimension chunks
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_DP, sdesc_sw128(sV + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(sDO + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
+          mma_ss(tmem + C::COL_S, sdesc_sw128(sK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(sQ(t) + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
       };
-      auto wait_q = [&](int t) {
-        return mbar_wait(qo_full, t & 1, ab) && mbar_wait(qw_full(t & 1), (t >> 1) & 1, ab);
+      auto issue_dp = [&](int t) {  // dP^T = V dO_t^T: A = V from TMEM (16 d = 8 columns per step)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tmem + C::COL_DP, tmem + C::COL_V + kk * 8,
+                 sdesc_sw128(sDO(t) + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
       };
-      auto wait_do = [&](int t) { return mbar_wait(doo_full, t & 1, ab) && mbar_wait(dow_full, t & 1, ab); };
-      bool ok = mbar_wait(kv_full, 0, ab) && wait_q(0);
+      bool ok = mbar_wait(k_full, 0, ab) && mbar_wait(st_full(0), 0, ab);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         mma_commit(s_full);
-        mma_commit(qo_empty);
-        ok = wait_do(0);
+        ok = mbar_wait(v_ready, 0, ab);
       }
       if (ok) {
         tc_fence_after();
-        issue_dp();
+        issue_dp(0);
         mma_commit(dp_full);
-        mma_commit(doo_empty);
       }
       for (int t = 0; ok && t < ntiles; ++t) {
         const uint32_t par = t & 1;
@@ -285,37 +235,35 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 32 * (kk >> 1) + (kk & 1) * 8,
-                 sdesc_sw128(sDO + 2 * hh * 8192 + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(dow_empty);
+                 sdesc_sw128(sDO(t) + 2 * hh * 8192 + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
         if (more) {  // S^T of the next tile over the P^T columns (the dV MMAs above read them first)
-          if (!(ok = wait_q(t + 1))) break;
+          if (!(ok = mbar_wait(st_full((t + 1) & 1), ((t + 1) >> 1) & 1, ab))) break;
           tc_fence_after();
           issue_s(t + 1);
           mma_commit(s_full);
-          mma_commit(qo_empty);
         }
         if (!(ok = mbar_wait(ds_ready, par, ab))) break;
-        if (t > 0 && !(ok = mbar_wait(dq_empty, par ^ 1, ab))) break;
         tc_fence_after();
-        // dQ^T_h = K[:, h]^T dS^T: A = K's chunks 2h, 2h+1 as MN-major [keys][d] (16 KB apart),
-        // B = dS^T [keys][64 queries] (MN-major)
+        // dQ^T_h = K[:, h]^T dS^T into the dP^T columns (read by the compute warps before
+        // ds_ready): A = K's chunks 2h, 2h+1 as MN-major [keys][d] (16 KB apart), B = dS^T
+        // [keys][64 queries] (MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::COL_DQ, sdesc_sw128(sK + 2 * hh * 16384 + kk * 2048, 16384, 1024),
+          mma_ss(tmem + C::COL_DP, sdesc_sw128(sK + 2 * hh * 16384 + kk * 2048, 16384, 1024),
                  sdesc_sw128(sDS + kk * 2048, 16384, 1024), idQ, kk > 0);
         mma_commit(dq_full);
-        // dK_h += dS^T Q[:, h]: A = dS^T (K-major over queries), B = this tile's own-half buffer
+        // dK_h += dS^T Q[:, h]: A = dS^T (K-major over queries), B = Q's chunks 2h, 2h+1
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + kk * 32, 16, 1024),
-                 sdesc_sw128(sQW(t) + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(qw_empty(t & 1));
-        if (more) {  // dP^T of the next tile (the compute warps have read dP^T(t): ds_ready)
-          if (!(ok = wait_do(t + 1))) break;
+                 sdesc_sw128(sQ(t) + 2 * hh * 8192 + kk * 2048, 8192, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(st_empty(t & 1));  // Q, dO and the lse2/D rows of this stage are free after these
+        if (more) {  // dP^T of the next tile, once dQ^T(t) has left the columns
+          if (!(ok = mbar_wait(dq_empty, par, ab) && mbar_wait(st_full((t + 1) & 1), ((t + 1) >> 1) & 1, ab)))
+            break;
           tc_fence_after();
-          issue_dp();
+          issue_dp(t + 1);
           mma_commit(dp_full);
-          mma_commit(doo_empty);
         }
       }
       mma_commit(mma_done);
@@ -324,23 +272,46 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------ compute: P^T and dS^T
+    // ------------------------------------------------------------ compute: V, then P^T and dS^T
     const int w = warp >> 2;           // query quarter: queries 32 w .. 32 w + 31 of the tile
     const int r = threadIdx.x & 127;   // key row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool key_pad = j * 128 + r >= p.Nk;
+    if (ntiles > 0) {
+      // V row r into TMEM (A operand of dP^T): warpgroup w writes head-dimension columns
+      // [128 w, 128 w + 128), two bf16 per 32-bit column; rows past Nk are zero
+      const uint4* vrow = static_cast<const uint4*>(p.v) + ((size_t)bg * p.Nk + (size_t)j * 128 + r) * (D / 8) + 16 * w;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const uint4 x = key_pad ? make_uint4(0u, 0u, 0u, 0u) : ld_nc_v4(vrow + 8 * half + m);
+          pk[4 * m] = x.x;
+          pk[4 * m + 1] = x.y;
+          pk[4 * m + 2] = x.z;
+          pk[4 * m + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_off + C::COL_V + 64 * w + 32 * half, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(v_ready);
+    }
     const uint32_t tS = tmem + lane_off + C::COL_S + 32 * w;
     const uint32_t tDP = tmem + lane_off + C::COL_DP + 32 * w;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t scx2 = f2_pack(p.scale, p.scale);
     uint8_t* ds_row = smem + C::OFF_DS + r * 128;
-    const bool key_pad = j * 128 + r >= p.Nk;
     for (int t = 0; t < ntiles; ++t) {
       // causal: key 128 j + r is masked for query 64 i + 32 w + c when c < cut
       const int cut = p.causal ? r + 128 * j - 64 * tile_row(t) - 32 * w - p.qoff : 0;
       const int s = t & 1;
+      // lse2/D of this stage: landed with the stage's copies, which the MMA warp waited for
+      // before S^T(t)
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512) + 8 * w;
       const float4* d4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512 + 256) + 8 * w;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, ab) && mbar_wait(ld_full(s), (t >> 1) & 1, ab))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, ab))) break;
       tc_fence_after();
       float pv[32];
       {
@@ -407,23 +378,30 @@ __global__ void __launch_bounds__(512, 1)
               make_uint4(pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2], pk[4 * pc + 3]);
         }
       }
-      fence_async_smem();
-      tc_fence_before();
+      fence_async_smem();  // dS^T visible to the MMAs (async proxy)
+      tc_fence_before();   // our TMEM loads of dP^T are done before dQ^T overwrites the columns
       mbar_arrive(ds_ready);
-      mbar_arrive(ld_empty(s));  // this stage's lse2/D rows are no longer read
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ read-out, dK/dV epilogue
     // dQ^T_h: TMEM lane L = head-dimension column 128 h + L, column c = query c of the tile
     const int L = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tDQ = tmem + lane_off + C::COL_DQ;
+    const uint32_t tDQ = tmem + lane_off + C::COL_DP;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int bh = tile_head(t), i = tile_row(t);
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, ab));
       if (!ok) break;
       tc_fence_after();
+      // hand the columns back to the MMA warp first: the next dP^T waits for them
+      uint32_t va[32], vb[32];
+      tmem_ld32_nowait(tDQ, va);
+      tmem_ld32_nowait(tDQ + 32, vb);
+      tmem_wait_ld(va);
+      tmem_wait_ld(vb);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
       // deterministic: one counter per (head, 64-row query tile, half); contributions in the
       // order of the schedule (ascending key tiles, or descending from the last one the query
       // tile sees)
@@ -443,13 +421,6 @@ __global__ void __launch_bounds__(512, 1)
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
       }
-      uint32_t va[32], vb[32];
-      tmem_ld32_nowait(tDQ, va);
-      tmem_ld32_nowait(tDQ + 32, vb);
-      tmem_wait_ld(va);
-      tmem_wait_ld(vb);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
       if (!p.deterministic || !*abort) {
         float* col = p.dq_acc + ((size_t)bh * Np + (size_t)i * 64) * D + 128 * hh + L;
 #pragma unroll
@@ -502,8 +473,8 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo64, const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tdo64, const BwdParams& p,
+                          cudaStream_t stream) {
   using C = Bwd256Cfg;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -516,7 +487,7 @@ cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const 
   }
   const long long blocks = 2LL * ((p.Nk + 127) / 128) * p.B * p.Hkv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  bwd256_kernel<<<dim3((unsigned)blocks), dim3(512), C::SMEM, stream>>>(tq64, tk, tv, tdo64, p);
+  bwd256_kernel<<<dim3((unsigned)blocks), dim3(512), C::SMEM, stream>>>(tq64, tk, tdo64, p);
   return cudaGetLastError();
 }
 

@@ -47,12 +47,13 @@ struct FwdParams {
 };
 
 struct BwdParams {
+  const void* v;      // bf16 [B,Hkv,Nk,d] (read with plain loads by the d = 256 kernel)
   void* dk;           // bf16 [B,Hkv,Nk,d]
   void* dv;           // bf16 [B,Hkv,Nk,d]
   float* dq_acc;      // fp32 [B,H,Nqp,d] dQ accumulator, rows padded to Nqp = Nq rounded up to 128 (workspace)
   const float* lse2;  // per padded query row LSE * log2(e) (workspace)
   const float* dvec;  // per padded query row D = sum_c dO_c O_c (workspace)
-  int* counters;      // deterministic mode: [B*H*(Nqp/128)] ordering counters (workspace)
+  int* counters;      // deterministic mode: ordering counters, [B*H*(Nqp/128)] ([B*H*(Nqp/64)*2] at d = 256)
   int B, H, Hkv, Nq, Nk;
   int qoff;           // causal: query row i sits at position i + qoff = i + Nk - Nq
   int causal;
@@ -102,9 +103,10 @@ cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_bwd_main_pair(const CUtensorMap& tq, const CUtensorMap& tq64, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdo64,
                                  const BwdParams& p, cudaStream_t stream);
-// d = 256: two CTAs per key tile, one per head-dimension half (tq64, tdo64: 64-row boxes)
-cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo64, const BwdParams& p, cudaStream_t stream);
+// d = 256: two CTAs per key tile, one per head-dimension half (tq64, tdo64: 64-row boxes;
+// V is read through p.v)
+cudaError_t launch_bwd256(const CUtensorMap& tq64, const CUtensorMap& tk, const CUtensorMap& tdo64,
+                          const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long heads, int N, int d, cudaStream_t stream);
 // The forward on CTA pairs (d = 128, one split, MUFU exponentials): tq and tv with 128-row
 // boxes, tk64 with a 64-row box.
