@@ -84,6 +84,20 @@ def check_register_split(report: dict) -> None:
                                "forward kernel would not add up" % (name, r["registers"], FWD_LAUNCH_REGISTERS))
 
 
+# Kernels that must compile without register spills: the default forward (MUFU exponentials,
+# every head dimension) and the backward main kernels.  The forward variants that move 6 or 8
+# of every 32 exponentials to the FMA polynomial (an option, measured slower) are exempt.
+NO_SPILL = (re.compile(r"fwd_kernelILi\d+ELi0E"), re.compile(r"bwd_main_kernel"), re.compile(r"bwd_pair_kernel"),
+            re.compile(r"bwd256_kernel"), re.compile(r"fwd_pair_kernel"), re.compile(r"fwd_fp8_kernel"))
+
+
+def check_spills(report: dict) -> None:
+    for name, r in report.items():
+        if any(pat.search(name) for pat in NO_SPILL) and (r["spill_stores"] or r["spill_loads"]):
+            raise RuntimeError("%s spills registers (%d bytes stored, %d loaded)"
+                               % (name, r["spill_stores"], r["spill_loads"]))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link the library if any source is newer than it; return its path."""
     if not force and not _stale():
@@ -110,7 +124,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join("%s:\n%s" % (s, t[-4000:]) for s, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    check_register_split(ptxas_report("\n".join(log)))
+    report = ptxas_report("\n".join(log))
+    check_register_split(report)
+    check_spills(report)
     tmp = LIB + ".tmp.%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     subprocess.run(cmd, check=True)

@@ -367,6 +367,17 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), jg & 1, ab));
         if (!ok) break;
         tc_fence_after();
+        const int col0 = (wu.j0 + j) * 128;
+        // column c of the tile is masked from lim on: past Nk, or (causal) after the row's position
+        const int lim = p.causal ? min(p.Nk - col0, rpos + p.qoff + 1 - col0) : p.Nk - col0;
+        // whether the tile needs the mask at all (a test on the tile's first row, or at d = 64, on
+        // the warp's rows: the forms that keep each instantiation free of register spills)
+        bool mask_tile;
+        if constexpr (D == 64) {
+          mask_tile = __any_sync(0xffffffffu, lim < 128);
+        } else {  // packed rows: the smallest position in the tile is 0 (+ qoff)
+          mask_tile = (p.causal && col0 + 127 > (p.pos_mod ? 0 : tile_row0) + p.qoff) || col0 + 128 > p.Nk;
+        }
         float s[128];
         {
           uint32_t rr[128];
@@ -374,14 +385,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
         }
-        const int col0 = (wu.j0 + j) * 128;
-        // packed rows: the smallest position in the tile is 0 (+ qoff)
-        if ((p.causal && col0 + 127 > (p.pos_mod ? 0 : tile_row0) + p.qoff) || col0 + 128 > p.Nk) {
+        if (mask_tile) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int col = col0 + c;
-            if ((p.causal && col > rpos + p.qoff) || col >= p.Nk) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
         }
         float mx4[4];
 #pragma unroll
@@ -406,13 +413,20 @@ __global__ void __launch_bounds__(384, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
             if (!ok) break;
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
+            auto rescale16 = [&](int c) {
               uint32_t rr[16];
               tmem_ld16(tO + 16 * c, rr);
 #pragma unroll
               for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
               tmem_st16(tO + 16 * c, rr);
+            };
+            if constexpr (D == 256) {
+              // a rolled loop: with the whole score row live, an unrolled one spills at d = 256
+#pragma unroll 1
+              for (int c = 0; c < D / 16; ++c) rescale16(c);
+            } else {
+#pragma unroll
+              for (int c = 0; c < D / 16; ++c) rescale16(c);
             }
             tmem_st_wait();
           }

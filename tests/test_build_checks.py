@@ -1,0 +1,43 @@
+"""Host checks of the build's ptxas gates: the forward kernel's register count (its setmaxnreg
+split assumes the launch holds exactly FWD_LAUNCH_REGISTERS per thread) and the kernels that
+must compile without register spills."""
+import pytest
+
+from exact_attention_49_gb300 import build
+
+REPORT = """
+ptxas info    : Compiling entry function '_ZN2fa10fwd_kernelILi128ELi0EEEv14CUtensorMap_stS1_S1_NS_9FwdParamsEi' for 'sm_103a'
+ptxas info    : Function properties for _ZN2fa10fwd_kernelILi128ELi0EEEv14CUtensorMap_stS1_S1_NS_9FwdParamsEi
+    %s bytes stack frame, %s bytes spill stores, %s bytes spill loads
+ptxas info    : Used %s registers, used 1 barriers
+ptxas info    : Compiling entry function '_ZN2fa10fwd_kernelILi128ELi8EEEv14CUtensorMap_stS1_S1_NS_9FwdParamsEi' for 'sm_103a'
+ptxas info    : Function properties for _ZN2fa10fwd_kernelILi128ELi8EEEv14CUtensorMap_stS1_S1_NS_9FwdParamsEi
+    72 bytes stack frame, 92 bytes spill stores, 160 bytes spill loads
+ptxas info    : Used 168 registers, used 1 barriers
+"""
+
+
+def report(stack=0, st=0, ld=0, regs=168):
+    return build.ptxas_report(REPORT % (stack, st, ld, regs))
+
+
+def test_parse():
+    r = report(8, 4, 36, 168)
+    k = [n for n in r if "ILi128ELi0E" in n][0]
+    assert r[k] == {"registers": 168, "spill_stores": 4, "spill_loads": 36}
+
+
+def test_clean_report_passes():
+    r = report()
+    build.check_register_split(r)
+    build.check_spills(r)  # the 8-of-32 polynomial split is exempt
+
+
+def test_spill_in_default_forward_fails():
+    with pytest.raises(RuntimeError, match="spills"):
+        build.check_spills(report(8, 4, 36))
+
+
+def test_wrong_register_count_fails():
+    with pytest.raises(RuntimeError, match="registers per thread"):
+        build.check_register_split(report(regs=160))
