@@ -58,21 +58,6 @@ struct Bwd2Cfg {
 };
 static_assert(Bwd2Cfg::SMEM <= 232448, "shared memory");
 
-FA_DEV void bulk_load2(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-FA_DEV void red_add2(float* addr, float a) { asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory"); }
-FA_DEV void red_add_release(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-FA_DEV int ld_acquire2(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-FA_DEV void named_bar2(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
     bwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q64,
@@ -196,8 +181,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
         if (!mbar_wait_cl(ld_empty(s), ((t >> 1) & 1) ^ 1, ab)) break;
         const size_t row0 = (size_t)bh * Np + (size_t)i * 128;
         mbar_arrive_expect_tx(ld_full(s), 1024);
-        bulk_load2(sbase + C::OFF_LD + s * 1024, p.lse2 + row0, 512, ld_full(s));
-        bulk_load2(sbase + C::OFF_LD + s * 1024 + 512, p.dvec + row0, 512, ld_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 1024, p.lse2 + row0, 512, ld_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 1024 + 512, p.dvec + row0, 512, ld_full(s));
         ok = mbar_wait_cl(qh_empty, pe, ab);
         if (ok && !skip) {
           if (rank == 0) mbar_arrive_expect_tx(qh_full, 2 * 16384);
@@ -461,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
       if (p.deterministic) {
         if (L == 0) {
           const uint64_t t0 = globaltimer();
-          while (ld_acquire2(counter) < 2 * rank_p) {
+          while (ld_acquire(counter) < 2 * rank_p) {
             const unsigned long long el = globaltimer() - t0;
             if (should_stop(ab, el)) break;
             if (el > kWaitLimitNs) {
@@ -470,7 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
             }
           }
         }
-        named_bar2(1, 128);
+        named_bar(1, 128);
       }
       uint32_t va[32], vb[32];
       tmem_ld32_nowait(tDQ, va);
@@ -485,13 +470,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(448, 1)
       if (!p.deterministic || !*abort) {
         float* col = p.dq_acc + ((size_t)bh * Np + (size_t)i * 128 + qbase) * D + dcol;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) red_add2(col + (size_t)m * D, __uint_as_float(va[m]));
+        for (int m = 0; m < 32; ++m) red_add(col + (size_t)m * D, __uint_as_float(va[m]));
 #pragma unroll
-        for (int m = 0; m < 32; ++m) red_add2(col + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
+        for (int m = 0; m < 32; ++m) red_add(col + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
       }
       if (p.deterministic) {
         __threadfence();
-        named_bar2(1, 128);
+        named_bar(1, 128);
         // (failure-injection test hook: the first pair keeps its successors waiting)
         if (L == 0 && !(p.debug_hook == 1 && cl == 0)) red_add_release(counter, 1);
       }

@@ -51,30 +51,6 @@ struct Bwd256Cfg {
   static constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_V = 384;
 };
 
-FA_DEV void bulk_load256(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-FA_DEV void red_add256(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-FA_DEV int ld_acquire256(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-FA_DEV void st_release256(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-FA_DEV uint4 ld_nc_v4(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __global__ void __launch_bounds__(512, 1)
     bwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -177,8 +153,8 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_3d(sbase + C::OFF_DO + s * C::STAGE + ch * 8192, &tm_do, st_full(s), ch * 64, i * 64, bh);
         }
         const size_t row0 = (size_t)bh * Np + (size_t)i * 64;
-        bulk_load256(sbase + C::OFF_LD + s * 512, p.lse2 + row0, 256, st_full(s));
-        bulk_load256(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row0, 256, st_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 512, p.lse2 + row0, 256, st_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row0, 256, st_full(s));
         issued = t + 1;
       }
       if (*abort) {  // let copies in flight land before the CTA exits (bounded)
@@ -410,7 +386,7 @@ __global__ void __launch_bounds__(512, 1)
       if (p.deterministic) {
         if (L == 0) {
           const uint64_t t0 = globaltimer();
-          while (ld_acquire256(counter) != rank) {
+          while (ld_acquire(counter) != rank) {
             const unsigned long long el = globaltimer() - t0;
             if (should_stop(ab, el)) break;
             if (el > kWaitLimitNs) {
@@ -419,19 +395,19 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        named_bar(1, 128);
       }
       if (!p.deterministic || !*abort) {
         float* col = p.dq_acc + ((size_t)bh * Np + (size_t)i * 64) * D + 128 * hh + L;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) red_add256(col + (size_t)m * D, __uint_as_float(va[m]));
+        for (int m = 0; m < 32; ++m) red_add(col + (size_t)m * D, __uint_as_float(va[m]));
 #pragma unroll
-        for (int m = 0; m < 32; ++m) red_add256(col + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
+        for (int m = 0; m < 32; ++m) red_add(col + (size_t)(32 + m) * D, __uint_as_float(vb[m]));
       }
       if (p.deterministic) {
         __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (L == 0 && !(p.debug_hook == 1 && blockIdx.x < 2)) st_release256(counter, rank + 1);
+        named_bar(1, 128);
+        if (L == 0 && !(p.debug_hook == 1 && blockIdx.x < 2)) st_release(counter, rank + 1);
       }
     }
     if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, ab));

@@ -432,6 +432,42 @@ FA_DEV uint64_t ex2_poly2(uint64_t x2) {
                  __uint_as_float(__float_as_uint(qq.y) + (__float_as_uint(tt.y) << 23)));
 }
 
+// ---- global-memory helpers of the backward kernels
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) completing on `bar`.
+FA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// fp32 reductions into global memory (performed at L2, no value returned)
+FA_DEV void red_add(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+FA_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+// ordering counters of the deterministic backward (GPU scope)
+FA_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+FA_DEV void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+FA_DEV void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// barrier `id` among `n` threads (a multiple of 32)
+FA_DEV void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// 16-byte load through the read-only path (data not written during the kernel)
+FA_DEV uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 FA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   // cvt.rn.bf16x2.f32 d, a, b puts a in the upper half and b in the lower half.
   uint32_t r;
