@@ -438,11 +438,15 @@ def run_ours(args, w):
     dom_ms = main_ms if dominant == "bwd_main" else fwd_ms
     dom_flops = f_bwd if dominant == "bwd_main" else f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    dom_kernel = {"fwd": "fwd_kernel<%d, 0>" % d,
-                  "bwd_main": "bwd256_kernel" if d == 256 else "bwd_main_kernel<%d>" % d}[dominant]
+    pair = d == 128 and fa.fa_get_option("bwd_2cta") == 1
+    bwd_kernel = ("bwd256_kernel" if d == 256 else "bwd_pair_kernel" if pair
+                  else "bwd_main_kernel<%d, %d>" % (d, det))
+    fwd_kernel = ("fwd_pair_kernel" if d == 128 and fa.fa_get_option("fwd_2cta") == 1
+                  else "fwd_kernel<%d, 0>" % d)
+    dom_kernel = {"fwd": fwd_kernel, "bwd_main": bwd_kernel}[dominant]
     roofline = {"bound": "tensor", "kernel": dom_kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": dram_traffic(dominant, w.name) if d == 128 and not det else None,
+                "traffic": dram_traffic(dominant, w.name) if d == 128 and not det and "pair" not in dom_kernel else None,
                 "peak_source": "%s %s (%s)" % (peak_src, peak_key, "MEASURED_PEAKS.json" if peak_src == "measured"
                                                else "profiling recipe fallback")}
 

@@ -91,11 +91,21 @@ NO_SPILL = (re.compile(r"fwd_kernelILi\d+ELi0E"), re.compile(r"bwd_main_kernel")
             re.compile(r"bwd256_kernel"), re.compile(r"fwd_pair_kernel"), re.compile(r"fwd_fp8_kernel"))
 
 
+# The exception: the backward's default instance at d = 128 reads a whole dQ column (128
+# values) before reducing it, so that tensor memory goes back to the MMA warp sooner; a few
+# values pass through local memory.  That measured 5-7% faster on the whole backward than the
+# spill-free form, so it has a budget (bytes stored and loaded) instead of zero.
+SPILL_BUDGET = ((re.compile(r"bwd_main_kernelILi128ELb0E"), 192),)
+
+
 def check_spills(report: dict) -> None:
     for name, r in report.items():
-        if any(pat.search(name) for pat in NO_SPILL) and (r["spill_stores"] or r["spill_loads"]):
-            raise RuntimeError("%s spills registers (%d bytes stored, %d loaded)"
-                               % (name, r["spill_stores"], r["spill_loads"]))
+        if not any(pat.search(name) for pat in NO_SPILL):
+            continue
+        budget = next((b for pat, b in SPILL_BUDGET if pat.search(name)), 0)
+        if r["spill_stores"] > budget or r["spill_loads"] > budget:
+            raise RuntimeError("%s spills registers (%d bytes stored, %d loaded; %d allowed)"
+                               % (name, r["spill_stores"], r["spill_loads"], budget))
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

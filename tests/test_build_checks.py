@@ -41,3 +41,14 @@ def test_spill_in_default_forward_fails():
 def test_wrong_register_count_fails():
     with pytest.raises(RuntimeError, match="registers per thread"):
         build.check_register_split(report(regs=160))
+
+
+def test_backward_default_instance_has_a_spill_budget():
+    text = REPORT.replace("fwd_kernelILi128ELi0E", "bwd_main_kernelILi128ELb0E") % (176, 172, 172, 128)
+    build.check_spills(build.ptxas_report(text))  # within the budget
+    with pytest.raises(RuntimeError, match="spills"):
+        build.check_spills(build.ptxas_report(REPORT.replace("fwd_kernelILi128ELi0E", "bwd_main_kernelILi128ELb0E")
+                                              % (400, 400, 400, 128)))
+    with pytest.raises(RuntimeError, match="spills"):  # the deterministic instance has none
+        build.check_spills(build.ptxas_report(REPORT.replace("fwd_kernelILi128ELi0E", "bwd_main_kernelILi128ELb1E")
+                                              % (8, 4, 4, 128)))
