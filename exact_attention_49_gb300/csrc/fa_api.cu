@@ -369,17 +369,21 @@ int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, 
 // K/V group are contiguous in q, o and lse, so they are taken as one head of g*Nq rows (query
 // row i of head h becomes row (h % g) * Nq + i, at causal position i + Nk - Nq): K and V are
 // then read once per group.  The key tiles are split over `splits` CTAs per 256-row block.
-static int splitkv_choice(int B, int H, int Hkv, int Nq, int Nk, int splits) {
+static int splitkv_choice(int B, int H, int Hkv, int Nq, int Nk, int d, int splits) {
   const int rows = (H / Hkv) * Nq;
-  const long long blocks = (long long)B * Hkv * ((rows + 255) / 256);
   const int n_kv = (Nk + 127) / 128;
   if (splits <= 0) {
-    // one CTA per SM at a time: minimise (waves) x (key tiles per CTA + a fixed cost of about
-    // two tiles for the CTA's prologue and epilogue)
+    // one CTA per SM slot at a time: minimise (waves) x (key tiles per CTA + a fixed cost of
+    // about two tiles for the CTA's prologue and epilogue).  With more than one split, units of
+    // at most 128 rows run in the decoding configuration: 128-row units, two CTAs per SM.
     const long long sms = sm_count_api();
+    const bool dec = fwd_decoding_config(d, rows, 2, 0);
     long long best = -1;
     for (int S = 1; S <= std::min(n_kv, 256); ++S) {
-      const long long waves = (blocks * S + sms - 1) / sms;
+      const bool two = dec && S > 1;
+      const long long blocks = (long long)B * Hkv * (two ? (rows + 127) / 128 : (rows + 255) / 256);
+      const long long slots = sms * (two ? 2 : 1);
+      const long long waves = (blocks * S + slots - 1) / slots;
       const long long cost = waves * ((n_kv + S - 1) / S + 2);
       if (best < 0 || cost < best) {
         best = cost;
@@ -392,7 +396,7 @@ static int splitkv_choice(int B, int H, int Hkv, int Nq, int Nk, int splits) {
 
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int splits) {
   if (check_shape(B, H, Hkv, Nq, d) || check_shape(B, H, Hkv, Nk, d) || splits < 0 || splits > 4096) return 0;
-  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, splits);
+  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, d, splits);
   if (S == 1) return 0;
   const size_t rows = (size_t)B * H * Nq;
   return ((size_t)S * rows * d * 4 + 255) / 256 * 256 + (size_t)S * rows * 4;
@@ -414,7 +418,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     return FA_ERR_MISALIGNED;
   const int g = H / Hkv;
   if ((long long)g * Nq > (1 << 30)) return FA_ERR_INVALID_ARG;
-  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, splits);
+  const int S = splitkv_choice(B, H, Hkv, Nq, Nk, d, splits);
   const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, Hkv, Nq, Nk, d, splits);
   if (S > 1) {
     if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;

@@ -40,7 +40,11 @@
 
 namespace fa {
 
-template <int D>
+// DEC: the decoding configuration (split-KV units of at most 128 query rows): one query tile,
+// 192 threads (one softmax warpgroup, the MMA warp and the TMA warp) and 256 tensor-memory
+// columns, so that two CTAs share an SM and their per-tile chains (S MMA -> softmax -> PV MMA)
+// overlap; one such chain per SM streams K/V well short of the HBM copy rate.
+template <int D, bool DEC = false>
 struct FwdCfg {
   static constexpr int BM = 128;                    // rows per query tile
   static constexpr int BN = 128;                    // keys per K/V tile
@@ -48,21 +52,30 @@ struct FwdCfg {
   static constexpr int CHUNKS = D / 64;             // 128-byte swizzle atoms across D
   // query tiles per work unit: two (S0 | S1 | O0 | O1 in TMEM), or one at d = 256 (S0 | O0
   // already take 384 of the 512 columns)
-  static constexpr int NT = (D == 256) ? 1 : 2;
+  static constexpr int NT = (DEC || D == 256) ? 1 : 2;
   static constexpr int BLOCK = 128 * NT;            // query rows per work unit
-  static constexpr int STAGES = (D == 256) ? 2 : (D == 128) ? 4 : 8;  // K/V ring slots
+  static constexpr int STAGES = DEC ? (D == 64 ? 4 : 2) : (D == 256) ? 2 : (D == 128) ? 4 : 8;  // K/V ring slots
   static constexpr int SMEM_Q = NT * TILE;
   static constexpr int SMEM_RING = STAGES * TILE;
   static constexpr int NBAR = 2 * STAGES + 11;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NBAR * 8 + 16;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = DEC ? 192 : 384;
+  static constexpr int SOFT_WARPS = DEC ? 4 : 8;     // softmax warps; the copy/MMA warps follow
+  static constexpr int MIN_BLOCKS = DEC ? 2 : 1;     // CTAs per SM
+  static constexpr int TMEM_COLS = DEC ? 256 : 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = (NT == 2) ? 256 : 128, COL_O1 = 256 + D;
   // Register split (setmaxnreg): the kernel is launched at 168 registers per thread (384
   // threads, 64512 registers); the two softmax warpgroups take 184 each, the copy/MMA
   // warpgroup keeps 136.  The shares must add up to the launch's total, or the increase waits
   // forever (build.py checks the compiled register count).
-  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 184, REG_OTHER = 136;
-  static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER == THREADS * REG_LAUNCH, "register split");
+  // The decoding configuration (one softmax warpgroup plus the MMA and TMA warps, 192 threads,
+  // two CTAs per SM) has no whole second warpgroup and so no split: every thread keeps the 168
+  // registers that two CTAs of 192 threads leave.
+  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = DEC ? 168 : 184, REG_OTHER = DEC ? 168 : 136;
+  static_assert(DEC || (SOFT_WARPS / 4) * 128 * REG_SOFTMAX + (THREADS / 128 - SOFT_WARPS / 4) * 128 * REG_OTHER ==
+                           THREADS * REG_LAUNCH,
+                "register split");
+  static_assert(!DEC || MIN_BLOCKS * THREADS * REG_LAUNCH <= 65536, "two CTAs per SM");
 };
 
 // One work unit: a block of BLOCK query rows of one (b, h) and, with split-KV, a key range.
@@ -74,9 +87,9 @@ struct FwdUnit {
 
 // Units are numbered heaviest first under a causal mask (the blocks nearest the end of the
 // sequence see the most keys), then by (b, h), then by split.
-template <int D>
+template <int D, bool DEC = false>
 FA_DEV FwdUnit fwd_unit(const FwdParams& p, int u) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DEC>;
   const int N = p.Nq;  // query rows; keys: p.Nk
   const int ncb = (N + C::BLOCK - 1) / C::BLOCK;
   const int BH = p.B * p.H;
@@ -114,11 +127,11 @@ FA_DEV int fwd_unit_index(int r) {
 
 // POLY: how many of every 16 column pairs take the FMA-pipe polynomial exp2 instead of
 // the MUFU ex2 unit (0 = MUFU only).
-template <int D, int POLY>
-__global__ void __launch_bounds__(384, 1)
+template <int D, int POLY, bool DEC = false>
+__global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_BLOCKS)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_units) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DEC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -159,11 +172,11 @@ __global__ void __launch_bounds__(384, 1)
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == C::SOFT_WARPS) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 9 && lane == 0) {
+  if (warp == C::SOFT_WARPS + 1 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -173,9 +186,9 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
-    if (warp == 9 && lane == 0) {
+  if (warp >= C::SOFT_WARPS) {
+    if constexpr (!DEC) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+    if (warp == C::SOFT_WARPS + 1 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       uint32_t it = 0;      // ring position of the next K/V load (continues across units)
       uint32_t issued = 0;  // ring loads issued
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int r = 0; ok; ++r) {
         const int u = fwd_unit_index(r);
         if (u >= n_units) break;
-        const FwdUnit w = fwd_unit<D>(p, u);
+        const FwdUnit w = fwd_unit<D, DEC>(p, u);
         // the Q buffer is free once the previous unit's last S MMAs have completed
         if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-    } else if (warp == 8 && lane == 0) {
+    } else if (warp == C::SOFT_WARPS && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int r = 0; ok; ++r) {
         const int u = fwd_unit_index(r);
         if (u >= n_units) break;
-        const FwdUnit w = fwd_unit<D>(p, u);
+        const FwdUnit w = fwd_unit<D, DEC>(p, u);
         ok = w.two ? unit_mma(w, std::true_type{}, it, units, units2, jg0, jg1)
                    : unit_mma(w, std::false_type{}, it, units, units2, jg0, jg1);
         it += 2 * w.n_kv;
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
+    if constexpr (!DEC) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int w = warp >> 2;            // query tile
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int ru = 0; ok; ++ru) {
       const int u = fwd_unit_index(ru);
       if (u >= n_units) break;
-      const FwdUnit wu = fwd_unit<D>(p, u);
+      const FwdUnit wu = fwd_unit<D, DEC>(p, u);
       if (w == 1 && !wu.two) continue;  // no row of this block falls in query tile 1
       const int row = wu.q0 + w * 128 + r;                 // absolute query row
       const int rpos = p.pos_mod ? row % p.pos_mod : row;  // its position for the causal mask
@@ -523,9 +536,9 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == C::SOFT_WARPS) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -541,24 +554,24 @@ static int fwd_sm_count() {
   return n[dev];
 }
 
-template <int D, int POLY>
+template <int D, int POLY, bool DEC = false>
 static cudaError_t launch_fwd_dp(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const FwdParams& p, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DEC>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fwd_kernel<D, POLY, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   const long long units = (long long)((p.Nq + C::BLOCK - 1) / C::BLOCK) * p.B * p.H * p.splits;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // persistent: one CTA per SM (at most one per unit)
-  const int grid = (int)std::min<long long>(units, fwd_sm_count());
-  fwd_kernel<D, POLY><<<dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p, (int)units);
+  // persistent: one CTA per SM (two in the decoding configuration), at most one per unit
+  const int grid = (int)std::min<long long>(units, (long long)fwd_sm_count() * C::MIN_BLOCKS);
+  fwd_kernel<D, POLY, DEC><<<dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tq, tk, tv, p, (int)units);
   return cudaGetLastError();
 }
 
@@ -575,8 +588,14 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
   }
 }
 
+bool fwd_decoding_config(int d, int rows, int splits, int poly_cols) {
+  return (d == 64 || d == 128) && poly_cols == 0 && splits > 1 && rows <= 128;
+}
+
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int poly_cols, cudaStream_t stream) {
+  if (fwd_decoding_config(d, p.Nq, p.splits, poly_cols))
+    return d == 64 ? launch_fwd_dp<64, 0, true>(tq, tk, tv, p, stream) : launch_fwd_dp<128, 0, true>(tq, tk, tv, p, stream);
   if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, poly_cols, stream);
   if (d == 256) {  // MUFU exponentials only at d = 256
     if (poly_cols != 0) return cudaErrorInvalidValue;

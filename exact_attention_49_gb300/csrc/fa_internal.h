@@ -122,6 +122,9 @@ cudaError_t launch_fwd_no_keys(void* o, float* lse, long long rows, int d, cudaS
 // exponentials on the FMA polynomial (0, 4, 8, 12 or 16).  Returns a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int poly_cols, cudaStream_t stream);
+// Whether launch_fwd takes the decoding configuration (two CTAs per SM, one query tile each):
+// split-KV launches (splits > 1) whose units hold at most 128 query rows, MUFU exponentials.
+bool fwd_decoding_config(int d, int rows, int splits, int poly_cols);
 constexpr int kDefaultPolyCols = 0;
 
 // Build a 3-D bf16 tensor map over a contiguous [outer][rows][d] array with a

@@ -7,7 +7,8 @@ fa_fwd_qk (bottom-right causal mask when Nq != Nk), so every case is compared
 with the fp64 oracle on every element: one decoding query, a few queries with
 a causal mask (per-row positions inside the packed block), MQA/GQA/MHA, d = 64
 and 128, ragged key counts, more splits than key tiles and the library's own
-split choice.
+split choice; blocks of up to 128 rows with more than one split run in the
+decoding configuration (two CTAs per SM), larger ones in the default form.
 """
 import numpy as np
 import pytest
@@ -40,6 +41,8 @@ CASES = [
     (2, 4, 4, 1, 128, 128, True, 16),
     (1, 32, 8, 1, 8192, 128, True, 64),
     (1, 4, 2, 200, 600, 64, True, 2),
+    (1, 32, 1, 4, 3000, 128, True, 0),   # 128 rows: the last size of the two-CTAs-per-SM form
+    (1, 43, 1, 3, 1500, 64, True, 4),    # 129 rows: the 256-row form with splits
 ]
 
 
