@@ -55,6 +55,7 @@ CASES = [
     (1, 2, 2, 512, 128, 64),
     (2, 4, 2, 300, 200, 128),
     (1, 2, 1, 640, 1280, 128),
+    (1, 2, 2, 500, 200, 128),  # causal: whole query tiles that see no key (dQ = 0 there)
 ]
 
 
