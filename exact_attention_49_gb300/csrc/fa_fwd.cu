@@ -64,6 +64,12 @@ struct FwdCfg {
   static constexpr int MIN_BLOCKS = DEC ? 2 : 1;     // CTAs per SM
   static constexpr int TMEM_COLS = DEC ? 256 : 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = (NT == 2) ? 256 : 128, COL_O1 = 256 + D;
+  // d = 256: S | O take 384 columns, so a second S buffer fits (columns 384-511).  Key tiles
+  // alternate between the two, so the next tile's S MMAs run while the softmax works on this
+  // one; K and V then come from two copy threads, so that a K load never queues behind a V
+  // slot the PV MMA still holds.
+  static constexpr bool DS = (D == 256 && !DEC);
+  static constexpr uint32_t COL_SB = 384;
   // Register split (setmaxnreg): the kernel is launched at 168 registers per thread (384
   // threads, 64512 registers); the two softmax warpgroups take 184 each, the copy/MMA
   // warpgroup keeps 136.  The shares must add up to the launch's total, or the increase waits
@@ -188,8 +194,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
 
   if (warp >= C::SOFT_WARPS) {
     if constexpr (!DEC) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
-    if (warp == C::SOFT_WARPS + 1 && lane == 0) {
+    if ((warp == C::SOFT_WARPS + 1 || (C::DS && warp == C::SOFT_WARPS + 2)) && lane == 0) {
       // ---------------------------------------------------------- TMA producer
+      // (with two S buffers: warp SOFT_WARPS + 1 loads Q and K, warp SOFT_WARPS + 2 loads V)
+      const bool do_k = !C::DS || warp == C::SOFT_WARPS + 1;
+      const bool do_v = !C::DS || warp == C::SOFT_WARPS + 2;
       uint32_t it = 0;      // ring position of the next K/V load (continues across units)
       uint32_t issued = 0;  // ring loads issued
       int q_loads = 0;   // Q loads issued (one per unit)
@@ -198,15 +207,18 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
         const int u = fwd_unit_index(r);
         if (u >= n_units) break;
         const FwdUnit w = fwd_unit<D, DEC>(p, u);
-        // the Q buffer is free once the previous unit's last S MMAs have completed
-        if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, ab)) break;
-        mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
-        for (int qt = 0; qt < C::NT; ++qt)
-          for (int ch = 0; ch < C::CHUNKS; ++ch)
-            tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, w.q0 + qt * 128, w.bh);
-        ++q_loads;
+        if (do_k) {
+          // the Q buffer is free once the previous unit's last S MMAs have completed
+          if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, ab)) break;
+          mbar_arrive_expect_tx(q_full, C::NT * C::TILE);
+          for (int qt = 0; qt < C::NT; ++qt)
+            for (int ch = 0; ch < C::CHUNKS; ++ch)
+              tma_load_3d(smem_u32(sQ + qt * C::TILE + ch * 16384), &tm_q, q_full, ch * 64, w.q0 + qt * 128, w.bh);
+          ++q_loads;
+        }
         for (int jj = 0; jj < 2 * w.n_kv; ++jj, ++it) {
           const int slot = it % C::STAGES;
+          if (!((jj & 1) ? do_v : do_k)) continue;  // the other copy thread's load
           if (r == 0 && jj == p.drop_it) continue;  // failure-injection test hook (never set in normal use)
           if (!mbar_wait(empty_bar(slot), ((it / C::STAGES) & 1) ^ 1, ab)) {
             ok = false;
@@ -223,6 +235,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
         // The CTA gave up: let the copies still in flight land before the CTA exits (each
         // completes its slot's phase), bounded at 1 ms per copy.
         for (uint32_t k = issued > C::STAGES ? issued - C::STAGES : 0; k < issued; ++k) {
+          if (!((k & 1) ? do_v : do_k)) continue;  // (two S buffers: the other thread's load)
           const uint64_t t0 = globaltimer();
           while (!mbar_try_wait(full_bar(k % C::STAGES), (k / C::STAGES) & 1) && globaltimer() - t0 < 1000000ull) {
           }
@@ -256,6 +269,23 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
           mma_ts(tmem + (w ? C::COL_O1 : C::COL_O0), tmem + sc + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
                  idO, (acc || kk > 0) ? 1u : 0u);
       };
+      // two S buffers (d = 256): Q against K in `slot` into the S columns `col`; O += P V
+      // with P read from the S columns `col`
+      auto issue_s_col = [&](uint32_t col, int slot) {
+        const uint32_t b0 = ring + slot * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + col, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idS, kk > 0);
+        }
+      };
+      auto issue_pv_col = [&](uint32_t col, int slot, bool acc) {
+        const uint32_t v0 = ring + slot * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::COL_O0, tmem + col + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024), idO,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
       auto slot_of = [](uint32_t k) { return k % C::STAGES; };
       auto par_of = [](uint32_t k) { return (k / C::STAGES) & 1u; };
       uint32_t it = 0;          // ring position (continues across units)
@@ -270,6 +300,41 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
                           const uint32_t u2_idx, const uint32_t g0, const uint32_t g1) -> bool {
         constexpr bool TWO = decltype(two_tiles)::value;
         const int n_kv = w.n_kv;
+        if constexpr (C::DS) {
+          // Key tile G (counted over the CTA's units) uses S buffer G & 1 and the barriers
+          // s_full / p_full / o_bar of that buffer.  S(G + 1) is issued before the wait for P(G),
+          // so it runs while the softmax works on tile G; P(G) in buffer G & 1 is read by PV(G)
+          // before S(G + 2) overwrites it (MMAs complete in issue order).
+          auto scol = [](uint32_t G) { return (G & 1) ? C::COL_SB : C::COL_S0; };
+          if (!mbar_wait(q_full, u_idx & 1, ab)) return false;
+          if (!mbar_wait(full_bar(slot_of(it0)), par_of(it0), ab)) return false;
+          tc_fence_after();
+          issue_s_col(scol(g0), slot_of(it0));
+          mma_commit(s_full(g0 & 1));
+          if (n_kv == 1) mma_commit(q_empty);
+          mma_commit(empty_bar(slot_of(it0)));
+          if (u_idx > 0 && !mbar_wait(o_free(0), (u_idx - 1) & 1, ab)) return false;
+          for (int j = 0; j < n_kv; ++j) {
+            const uint32_t G = g0 + j;
+            if (j + 1 < n_kv) {
+              const uint32_t itk = it0 + 2 * (j + 1);
+              if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), ab)) return false;
+              tc_fence_after();
+              issue_s_col(scol(G + 1), slot_of(itk));
+              mma_commit(s_full((G + 1) & 1));
+              if (j + 2 == n_kv) mma_commit(q_empty);
+              mma_commit(empty_bar(slot_of(itk)));
+            }
+            const uint32_t itv = it0 + 2 * j + 1;
+            if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), ab)) return false;
+            if (!mbar_wait(p_full(G & 1), (G >> 1) & 1, ab)) return false;
+            tc_fence_after();
+            issue_pv_col(scol(G), slot_of(itv), j > 0);
+            mma_commit(o_bar(G & 1));
+            mma_commit(empty_bar(slot_of(itv)));
+          }
+          return true;
+        }
         if (!mbar_wait(q_full, u_idx & 1, ab)) return false;
         if (!mbar_wait(full_bar(slot_of(it0)), par_of(it0), ab)) return false;
         tc_fence_after();
@@ -377,7 +442,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
       float lr0 = 0.f, lr1 = 0.f;
       const int tile_row0 = wu.q0 + w * 128;
       for (int j = 0; j < wu.n_kv; ++j, ++jg) {
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), jg & 1, ab));
+        // (two S buffers: key tile jg uses buffer jg & 1 and that buffer's barriers)
+        const int sb = C::DS ? (jg & 1) : w;
+        const uint32_t tSj = C::DS ? (tmem + lane_off + ((jg & 1) ? C::COL_SB : C::COL_S0)) : tS;
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(sb), C::DS ? ((jg >> 1) & 1) : (jg & 1), ab));
         if (!ok) break;
         tc_fence_after();
         const int col0 = (wu.j0 + j) * 128;
@@ -394,7 +462,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
         float s[128];
         {
           uint32_t rr[128];
-          tmem_ld128(tS, rr);  // one load and one wait for the whole row
+          tmem_ld128(tSj, rr);  // one load and one wait for the whole row
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
         }
@@ -423,7 +491,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
               if (lane == 0) atomicAdd(p.rescale_events, (unsigned long long)__popc(moved));
             }
             // O holds sum_{j'<j} P V against m_used; it must be complete before rescaling
-            ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
+            // (two S buffers: the previous tile's PV commits to its buffer's o_bar)
+            ok = __all_sync(0xffffffffu, mbar_wait(o_bar(C::DS ? ((jg - 1) & 1) : w),
+                                                   C::DS ? (((jg - 1) >> 1) & 1) : ((jg - 1) & 1), ab));
             if (!ok) break;
             tc_fence_after();
             auto rescale16 = [&](int c) {
@@ -474,17 +544,18 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
             else
               lr0 = add_bf16_hi(add_bf16_lo(lr0, pk[i]), pk[i]);
           }
-          tmem_st16(tS + 16 * c, pk);
+          tmem_st16(tSj + 16 * c, pk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(w));
+        mbar_arrive(p_full(sb));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE = ln 2 * (m_used + log2 l).  O's tensor memory is
       // handed back (o_free) right after the last load from it, so the next unit's first PV
       // MMA can overwrite it while these stores drain.
-      ok = __all_sync(0xffffffffu, mbar_wait(o_bar(w), (jg - 1) & 1, ab));
+      ok = __all_sync(0xffffffffu, mbar_wait(o_bar(C::DS ? ((jg - 1) & 1) : w),
+                                             C::DS ? (((jg - 1) >> 1) & 1) : ((jg - 1) & 1), ab));
       if (!ok) break;
       tc_fence_after();
       const float2 le = f2_unpack(l_exact);

@@ -1,6 +1,7 @@
 """GPU parity of the d = 256 forward (one 128-row query tile per CTA: S and O take
-384 of the 512 TMEM columns) against the fp64 oracle, element by element: square
-and non-square shapes, causal and not, ragged N, GQA, and split-KV decoding."""
+384 of the 512 TMEM columns, and a second S buffer the rest) against the fp64
+oracle, element by element: square and non-square shapes, causal and not, ragged
+N, GQA, CTAs that run several units, and split-KV decoding."""
 import numpy as np
 import pytest
 import torch
@@ -29,6 +30,10 @@ def _lib():
     (2, 4, 2, 512, 512, True),
     (1, 2, 2, 100, 700, True),
     (1, 2, 1, 640, 200, True),
+    # more units than SMs: each CTA runs several units, so the alternation of the two S
+    # buffers carries across units (key-tile counts odd and even)
+    (1, 32, 8, 1536, 1536, True),
+    (1, 24, 24, 1000, 1000, False),
 ])
 def test_fwd_d256(case):
     B, H, Hkv, Nq, Nk, causal = case
