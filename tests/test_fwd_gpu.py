@@ -91,6 +91,15 @@ def test_fwd_ragged(N, causal):
         check_full(1, 3, 1, N, d, causal, seed=N)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_many_units_ragged(causal, d):
+    """More units than SMs, with a ragged last block per head (a one-tile unit after two-tile
+    ones in the same CTA): at d = 64 the three S buffers rotate over the S MMAs of every unit,
+    and the rotation continues across units of both kinds."""
+    check_full(2, 40, 8, 1100, d, causal, seed=11 + d)
+
+
 def test_fwd_empty():
     z = torch.empty(0, dtype=torch.bfloat16, device="cuda")
     assert fa.fa_fwd(z, z, z, z, z, 1, 2, 2, 0, 64, 1, 0.125) == fa.FA_OK
