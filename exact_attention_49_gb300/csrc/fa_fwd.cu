@@ -355,23 +355,18 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
         }
         // one key tile; MORE: another tile follows (the last iteration is peeled so that the
         // test is not a run-time branch of the issue loop)
-        // T0: query tile 0 takes this key tile's PV and the next key tile's S.  A key tile that
-        // lies wholly after tile 0's rows (the last one of a causal two-tile unit) gets neither:
-        // the barriers are committed without MMAs, and the softmax finds every column masked
-        // (P = 0), so the phases and the result are those of the full schedule.
-        auto step = [&](int j, auto more_tiles, auto t0_pv, auto t0_s) -> bool {
+        auto step = [&](int j, auto more_tiles) -> bool {
           constexpr bool MORE = decltype(more_tiles)::value;
-          constexpr bool PV0 = decltype(t0_pv)::value, S0N = decltype(t0_s)::value;
           const uint32_t itv = it0 + 2 * j + 1, itk = itv + 1;
           if (!mbar_wait(full_bar(slot_of(itv)), par_of(itv), ab)) return false;
           if (!mbar_wait(p_full(0), (g0 + j) & 1, ab)) return false;
           tc_fence_after();
-          if constexpr (PV0) issue_pv(0, slot_of(itv), j > 0);
+          issue_pv(0, slot_of(itv), j > 0);
           mma_commit(o_bar(0));
           if constexpr (MORE) {
             if (!mbar_wait(full_bar(slot_of(itk)), par_of(itk), ab)) return false;
             tc_fence_after();
-            if constexpr (S0N) issue_s(0, slot_of(itk));
+            issue_s(0, slot_of(itk));
             mma_commit(s_full(0));
           }
           if constexpr (TWO) {
@@ -391,21 +386,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DEC>::THREADS, FwdCfg<D, DEC>::MIN_B
           }
           return true;
         };
-        using T_ = std::true_type;
-        using F_ = std::false_type;
         bool ok = true;
-        // the unit's last key tile lies wholly after query tile 0's rows (causal, rows at their
-        // own positions): tile 0 skips its MMAs
-        const bool skip0 = TWO && p.causal && !p.pos_mod && n_kv > 1 &&
-                           (w.j0 + n_kv - 1) * 128 > w.q0 + 127 + p.qoff;
-        if (skip0) {
-          for (int j = 0; ok && j + 2 < n_kv; ++j) ok = step(j, T_{}, T_{}, T_{});
-          if (ok) ok = step(n_kv - 2, T_{}, T_{}, F_{});
-          if (ok) ok = step(n_kv - 1, F_{}, F_{}, F_{});
-          return ok;
-        }
-        for (int j = 0; ok && j + 1 < n_kv; ++j) ok = step(j, T_{}, T_{}, T_{});
-        if (ok) ok = step(n_kv - 1, F_{}, T_{}, F_{});
+        for (int j = 0; ok && j + 1 < n_kv; ++j) ok = step(j, std::true_type{});
+        if (ok) ok = step(n_kv - 1, std::false_type{});
         return ok;
       };
       bool ok = true;
