@@ -6,8 +6,7 @@ wait is only right while the barrier is at most one phase away from the phase it
 beyond that it passes early or blocks forever.  The kernel's comments state, per wait, why
 that window holds (e.g. "S(G) complete implies PV(G - 2) complete").  This test replays the
 MMA issue order and the softmax loop of `fwd_kernel` (two query tiles per unit, including
-one-tile units and the causal unit's last key tile that query tile 0 skips; and the d = 256
-schedule with two S buffers).  MMAs complete in issue order after random delays; the
+one-tile units in the same CTA; and the d = 256 schedule with two S buffers).  MMAs complete in issue order after random delays; the
 scheduler starves one role at a time.  At every parity wait the test asserts that the barrier
 is exactly at the awaited phase, and it asserts that no run deadlocks.
 """
@@ -45,8 +44,7 @@ def units_of_cta(cta, grid, bh, n, causal, rows_per_unit):
         last = min(q0 + rows_per_unit - 1, n - 1)
         n_kv = min(n_kv_all, last // 128 + 1) if causal else n_kv_all
         two = rows_per_unit == 256 and n - q0 > 128
-        skip0 = two and causal and n_kv > 1 and (n_kv - 1) * 128 > q0 + 127
-        out.append(dict(n=max(1, n_kv), two=two, skip0=skip0))
+        out.append(dict(n=max(1, n_kv), two=two))
         r += 1
 
 
@@ -131,7 +129,7 @@ def two_tile_agents(m, units):
         it = nu = nu2 = 0
         g = [0, 0]
         for u in units:
-            n, two, skip0, it0 = u["n"], u["two"], u["skip0"], it
+            n, two, it0 = u["n"], u["two"], it
             yield m.wait(m.q_full, nu)
             yield m.wait(m.full[it0 % S], it0 // S)
             m.commit([m.s_full[0]])
@@ -149,10 +147,10 @@ def two_tile_agents(m, units):
                 itv, itk = it0 + 2 * j + 1, it0 + 2 * j + 2
                 yield m.wait(m.full[itv % S], itv // S)
                 yield m.wait(m.p_full[0], g[0] + j)
-                m.commit([m.o_bar[0]])  # PV0 (or, on tile 0's skipped tile, no MMA)
+                m.commit([m.o_bar[0]])  # PV0(j)
                 if more:
                     yield m.wait(m.full[itk % S], itk // S)
-                    m.commit([m.s_full[0]])  # S0(j + 1) (or no MMA before the skipped tile)
+                    m.commit([m.s_full[0]])  # S0(j + 1)
                 if two:
                     yield m.wait(m.p_full[1], g[1] + j)
                     m.commit([m.o_bar[1]])
